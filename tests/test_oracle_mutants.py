@@ -1,0 +1,137 @@
+"""The oracle's pins must catch plausible mistakes.  Each test plants one
+mistake in the oracle (on the CPU, through monkeypatching the oracle module)
+and checks that at least one pin from tests/test_oracle_*.py then fails."""
+import numpy as np
+import pytest
+
+import oracle.tree_verify as tv
+from tests import test_oracle_accept as acc
+from tests import test_oracle_attention as att
+from tests import test_oracle_compact as cmp
+
+
+def _fails(fn, *args):
+    try:
+        fn(*args)
+    except (AssertionError, ValueError, IndexError, KeyError):
+        return True
+    return False
+
+
+def _attention_pins(golden_dir):
+    return [
+        lambda: att.check_worked_examples(golden_dir),
+        lambda: att.check_chain_is_causal(0, 37, 9),
+        lambda: att.check_single_node_is_decode(0, 100),
+        lambda: att.check_node_is_attention_over_own_path(0),
+    ]
+
+
+def _some_fail(pins):
+    return any(_fails(p) for p in pins)
+
+
+def test_pins_pass_unmutated(golden_dir):
+    assert not _some_fail(_attention_pins(golden_dir))
+
+
+def test_exclusive_self_is_caught(monkeypatch, golden_dir):
+    orig = tv.ancestors_inclusive
+    monkeypatch.setattr(tv, "ancestors_inclusive", lambda parent, i: orig(parent, i)[1:])
+    assert _some_fail(_attention_pins(golden_dir))
+
+
+def test_wrong_gqa_map_is_caught(monkeypatch, golden_dir):
+    monkeypatch.setattr(tv, "kv_head_of", lambda h, hq, hkv: h % hkv)
+    assert _some_fail(_attention_pins(golden_dir))
+
+
+def test_wrong_scale_is_caught(monkeypatch, golden_dir):
+    monkeypatch.setattr(tv, "default_scale", lambda d: 1.0 / d)
+    assert _some_fail(_attention_pins(golden_dir))
+
+
+def test_parent_only_mask_is_caught(monkeypatch, golden_dir):
+    # a node that sees itself and its parent but not the rest of its path
+    def two_levels(parent, i):
+        return [i] + ([int(parent[i])] if parent[i] >= 0 else [])
+    monkeypatch.setattr(tv, "ancestors_inclusive", two_levels)
+    assert _some_fail(_attention_pins(golden_dir))
+
+
+def test_transposed_qk_is_caught(monkeypatch, golden_dir):
+    real = tv.tree_attention
+
+    def mutant(q, k, v, P, parent, scale=None):
+        q = np.asarray(q, dtype=np.float64)
+        # heads and nodes swapped when the shapes allow it
+        if q.shape[0] == q.shape[1]:
+            q = q.transpose(1, 0, 2).copy()
+        return real(q, k, v, P, parent, scale)
+    monkeypatch.setattr(att.oracle, "tree_attention", mutant)
+    pins = _attention_pins(golden_dir) + [lambda: att.check_chain_is_causal(1, 5, 4, hq=4, hkv=2)]
+    assert _some_fail(pins)
+
+
+def _accept_pins(golden_dir):
+    return [
+        lambda: acc.check_accept_worked_examples(golden_dir),
+        lambda: acc.check_bruteforce_small_trees(max_n=5, trials=2),
+    ]
+
+
+def test_highest_index_tie_is_caught(monkeypatch, golden_dir):
+    def walk(am, token, parent):
+        path = [0]
+        while True:
+            u = path[-1]
+            m = [c for c in range(len(parent)) if parent[c] == u and token[c] == am[u]]
+            if not m:
+                return path
+            path.append(max(m))
+    monkeypatch.setattr(tv, "greedy_walk", walk)
+    assert _some_fail(_accept_pins(golden_dir))
+
+
+def test_wrong_bonus_token_is_caught(monkeypatch, golden_dir):
+    monkeypatch.setattr(tv, "accepted_tokens",
+                        lambda path, am, token: [int(token[a]) for a in path[1:]] + [int(am[path[0]])])
+    assert _some_fail(_accept_pins(golden_dir))
+
+
+def test_new_parent_off_by_one_is_caught(monkeypatch, golden_dir):
+    real = tv.reroot
+
+    def mutant(parent, path, P):
+        new_pos, new_parent, r = real(parent, path, P)
+        new_parent = np.where(new_parent >= 0, new_parent + 1, new_parent)
+        return new_pos, new_parent, r
+    monkeypatch.setattr(tv, "reroot", mutant)
+    assert _fails(acc.check_accept_worked_examples, golden_dir)
+
+
+def test_inclusive_survivors_is_caught(monkeypatch, golden_dir):
+    real = tv.strict_descendants
+    monkeypatch.setattr(tv, "strict_descendants", lambda parent, u: [u] + real(parent, u))
+    assert _fails(acc.check_accept_worked_examples, golden_dir)
+
+
+def test_compaction_from_wrong_row_is_caught(monkeypatch):
+    def mutant(cache, P, new_pos):
+        old = np.asarray(cache)
+        new = old.copy()
+        for i, pos in enumerate(new_pos):
+            if pos >= 0:
+                new[..., pos, :] = old[..., P + i - 1 if i else P, :]
+        return new
+    monkeypatch.setattr(cmp.oracle, "kv_compact", mutant)
+    assert _fails(cmp.test_compaction_is_a_permutation_copy, 1) or \
+        _fails(cmp.test_reroot_preserves_survivor_attention)
+
+
+def test_last_occurrence_argmax_is_caught(monkeypatch):
+    def mutant(logits):
+        x = np.asarray(logits)
+        return (x.shape[1] - 1 - np.argmax(x[:, ::-1], axis=1)).astype(np.int32)
+    monkeypatch.setattr(acc.oracle, "target_argmax", mutant)
+    assert _fails(acc.test_argmax_ties_and_nan_follow_first_occurrence)
