@@ -1,0 +1,451 @@
+"""Benchmark of the full tree-verification step on GB300.
+
+One step = the whole verification hot path over one batch of synthetic input
+at 70B-class shapes (64 query / 8 KV heads, head dim 128, bf16, prefix 4096,
+a 64-node draft tree grown by 8 expansions of width 8): tree-masked attention
+for each of 80 layers, greedy acceptance against the target's argmax over a
+128256-token vocabulary, and in-place KV compaction of all 80 layers.  The
+step is captured once as a CUDA graph and replayed.  The KV caches (1.36 GB)
+are larger than L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same step instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "full_step"
+LAYERS, PREFIX, NODES, HQ, HKV, D, VOCAB = 80, 4096, 64, 64, 8, 128, 128256
+
+
+def _algorithmic_work(parent, prefix, n, hq, hkv, d, elem=2):
+    """Bytes and flops of one layer of tree attention (partials + combine),
+    counting only visible keys: K and V rows read once, Q read and O written
+    once; 4*d flops per visible (row, key) pair (QK^T and PV)."""
+    from workloads import synth
+    anc_total = int((synth.node_depths(parent) + 1).sum())  # |anc*(i)| = depth(i) + 1
+    bytes_ = 2 * hkv * (prefix + n) * d * elem + 2 * n * hq * d * elem
+    flops = 4 * hq * d * (n * prefix + anc_total)
+    return bytes_, flops
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p["bf16_tflops_sustained"], "source": "measured",
+                "sm_max_mhz": p.get("sm_max_mhz", 2070.0)}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback", "sm_max_mhz": 2070.0}
+
+
+def _kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_tree_masked_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith("attn") or name in ("common.cuh", "internal.h"):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic():
+    """DRAM bytes per attention launch from the committed ncu summary, if it
+    was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "attention_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if "=" in line and not line.startswith("#"):
+                k, v = line.split("=", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha") != _kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_layer"])
+    except (KeyError, ValueError):
+        return None
+
+
+class _Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self, sm_max_default):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": sm_max_default, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": sm_max_default, "reasons": ["unsampled"]}
+        busy = sorted(sm)[len(sm) // 2:] or sm  # the busier half of the samples
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle sample (the cpu_baseline leg and the reference arm)
+# --------------------------------------------------------------------------
+
+def oracle_sample(nodes: int, layers: int, seed: int = 0) -> dict:
+    """Times the oracle on a bounded sample of one verify step and scales it
+    to the full step: attention for `nodes` tree nodes of `layers` layers,
+    acceptance over the full logits, compaction of `layers` layers."""
+    import numpy as np
+    import oracle
+    from workloads import synth
+    w = synth.make_workload(WORKLOAD, seed=seed, layers=layers)
+    sample_nodes = list(range(0, NODES, max(1, NODES // nodes)))[:nodes]
+    t_attn = 0.0
+    t_comp = 0.0
+    t0 = time.perf_counter()
+    res = oracle.tree_accept(w.logits, w.token, w.parent, w.prefix)
+    t_acc = time.perf_counter() - t0
+    for layer in range(layers):
+        q, k, v = synth.make_qkv(w, layer=layer)
+        qn, kn, vn = q.float().numpy(), k.float().numpy(), v.float().numpy()
+        t0 = time.perf_counter()
+        oracle.tree_attention(qn, kn, vn, w.prefix, w.parent, nodes=sample_nodes)
+        t_attn += time.perf_counter() - t0
+        kb = k.view(torch_int16()).numpy()
+        vb = v.view(torch_int16()).numpy()
+        t0 = time.perf_counter()
+        oracle.kv_compact(kb, w.prefix, res["new_pos"])
+        oracle.kv_compact(vb, w.prefix, res["new_pos"])
+        t_comp += time.perf_counter() - t0
+    per_node_layer = t_attn / (len(sample_nodes) * layers)
+    t_step = per_node_layer * NODES * LAYERS + t_acc + (t_comp / layers) * LAYERS
+    return {"t_step_s": t_step, "sample_s": t_attn + t_comp + t_acc,
+            "sample": f"attention of {len(sample_nodes)} of {NODES} tree nodes x {layers} of "
+                      f"{LAYERS} layers, full acceptance, compaction of {layers} of {LAYERS} "
+                      f"layers; scaled to one full step", "threads": 1, "m": int(res["m"])}
+
+
+def torch_int16():
+    import torch
+    return torch.int16
+
+
+def _oracle_subprocess(nodes, layers, repeats):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps([bench.oracle_sample(%d, %d, seed=r) for r in range(%d)]))"
+            % (ROOT, nodes, layers, repeats))
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                         timeout=1800)
+    if out.returncode != 0:
+        raise RuntimeError("oracle sample failed: " + out.stderr[-2000:])
+    return json.loads(out.stdout.strip().splitlines()[-1])
+
+
+def _line_base(args, n_gpus):
+    return {
+        "metric": "tree-verify tokens/s", "unit": "tree tokens/s", "n_gpus": n_gpus,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 Q/K/V, "
+        "planted target argmax, max-likelihood-style tree)",
+        "config": {"workload": "full verify step, 70B-class: 64/8 heads, d128, bf16, prefix "
+                   "4096, 64-node tree (8 expansions of width 8), 80 layers, vocab 128256",
+                   "layers": LAYERS, "prefix": PREFIX, "tree_nodes": NODES, "hq": HQ,
+                   "hkv": HKV, "d": D, "vocab": VOCAB,
+                   "l2": "inputs larger than L2 (1.36 GB of KV per step), no flush",
+                   "parallelism": f"replicas x{n_gpus}"},
+    }
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    nodes, layers = 4, 1
+    samples = _oracle_subprocess(nodes, layers, args.warmup + args.steps)
+    timed = samples[args.warmup:]
+    t = statistics.mean(s["t_step_s"] for s in timed)
+    line = _line_base(args, world)
+    v = NODES / t
+    line.update({"impl": "reference", "value": v, "ms_per_step": t * 1e3, "dtype": "f64",
+                 "cpu_baseline": {"value": v, "unit": "tree tokens/s", "cores": 1,
+                                  "kind": "oracle", "sample": timed[0]["sample"]},
+                 "e2e": {"value": v, "unit": "tree tokens/s", "h2d_bytes_per_step": 0,
+                         "d2h_bytes_per_step": 0}})
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# the GPU arm
+# --------------------------------------------------------------------------
+
+def run_gpu(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import speculative_decoding_tree_masked_gb300 as tvp
+    from workloads import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = synth.make_workload(WORKLOAD, seed=args.seed + rank, layers=LAYERS)
+    cap = w.cap
+    # inputs resident in HBM
+    kc = torch.empty((LAYERS, HKV, cap, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    q = torch.empty((LAYERS, NODES, HQ, D), dtype=torch.bfloat16, device=dev)
+    for layer in range(LAYERS):
+        ql, kl, vl = synth.make_qkv(w, layer=layer)
+        q[layer].copy_(ql)
+        kc[layer].copy_(kl)
+        vc[layer].copy_(vl)
+    logits = torch.from_numpy(w.logits).to(dev)
+    token = torch.from_numpy(w.token).to(dev)
+    parent = torch.from_numpy(w.parent).to(dev)
+    out = torch.empty((LAYERS, NODES, HQ, D), dtype=torch.bfloat16, device=dev)
+    ws = tvp.attn_workspace(NODES, HQ, HKV, D, torch.bfloat16, PREFIX, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    acc = {k: torch.empty(sz, dtype=torch.int32, device=dev) for k, sz in (
+        ("am", NODES), ("m", 1), ("path", NODES), ("out_tokens", NODES + 1),
+        ("new_pos", NODES), ("new_parent", NODES), ("n_survivors", 1))}
+    stream = torch.cuda.Stream(dev)
+
+    def step(qs=q, lg=logits, tk=token, pr=parent):
+        for layer in range(LAYERS):
+            tvp.tree_attn_verify(qs[layer], kc[layer], vc[layer], PREFIX, pr, out=out[layer],
+                                 workspace=ws, status=status)
+        tvp.tree_accept(lg, tk, pr, PREFIX, outs=acc, status=status)
+        tvp.kv_compact(kc, vc, PREFIX, NODES, acc["new_pos"], status=status)
+
+    def attention_only():
+        for layer in range(LAYERS):
+            tvp.tree_attn_verify(q[layer], kc[layer], vc[layer], PREFIX, parent, out=out[layer],
+                                 workspace=ws, status=status)
+
+    with torch.cuda.stream(stream):
+        step()  # first calls: function attributes, SM count, driver entry points
+        attention_only()
+    torch.cuda.synchronize()
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=stream):
+        step()
+    g_attn = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_attn, stream=stream):
+        attention_only()
+    torch.cuda.synchronize()
+    launches_per_step = LAYERS * 2 + 2 + 1  # attention + combine per layer, argmax, walk, compact
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g_step.replay()
+    barrier()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    with _Clocks(local_rank) as clk:
+        barrier()
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            for i in range(args.steps):
+                g_step.replay()
+                ev[i + 1].record(stream)
+        barrier()
+    per_step = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+
+    # the dominant kernel alone: 80 layers of attention, events on its stream
+    reps = max(3, args.steps)
+    with torch.cuda.stream(stream):
+        g_attn.replay()
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        for _ in range(reps):
+            g_attn.replay()
+        eb.record(stream)
+    torch.cuda.synchronize()
+    attn_ms_layer = ea.elapsed_time(eb) / (reps * LAYERS)
+
+    # end to end through the public API: step inputs from pinned host memory,
+    # the step's result read back
+    q_h = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    q_h.copy_(q.cpu())
+    lg_h = torch.from_numpy(w.logits).pin_memory()
+    tk_h = torch.from_numpy(w.token).pin_memory()
+    pr_h = torch.from_numpy(w.parent).pin_memory()
+    q_d, lg_d, tk_d, pr_d = torch.empty_like(q), torch.empty_like(logits), torch.empty_like(
+        token), torch.empty_like(parent)
+    res_h = {k: torch.empty(acc[k].shape, dtype=torch.int32, pin_memory=True)
+             for k in ("m", "out_tokens", "new_pos", "n_survivors")}
+    g_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        step(q_d, lg_d, tk_d, pr_d)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g_e2e, stream=stream):
+        step(q_d, lg_d, tk_d, pr_d)
+    h2d = sum(x.numel() * x.element_size() for x in (q_h, lg_h, tk_h, pr_h))
+    d2h = sum(x.numel() * x.element_size() for x in res_h.values())
+    barrier()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            q_d.copy_(q_h, non_blocking=True)
+            lg_d.copy_(lg_h, non_blocking=True)
+            tk_d.copy_(tk_h, non_blocking=True)
+            pr_d.copy_(pr_h, non_blocking=True)
+            g_e2e.replay()
+            for k, hbuf in res_h.items():
+                hbuf.copy_(acc[k], non_blocking=True)
+            stream.synchronize()
+            _ = int(res_h["m"][0])  # the host reads the result
+    e2e_s = time.perf_counter() - t0
+    te = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_s = float(te.item())
+
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during the benchmark")
+    m_acc = int(acc["m"].item())
+
+    if rank != 0:
+        return
+    peaks = _peaks()
+    nbytes, flops = _algorithmic_work(w.parent, PREFIX, NODES, HQ, HKV, D)
+    t_layer = attn_ms_layer * 1e-3
+    gbs = nbytes / t_layer / 1e9
+    tflops = flops / t_layer / 1e12
+    tensor_path = tvp.lib().tv_attn_uses_tensor_cores(tvp.TV_BF16) != 0
+    if tensor_path:
+        roof = {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    else:
+        # fp32 FMA pipes: 152 SMs x 128 lanes x 2 flops x max SM clock
+        alu_peak = 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": tflops, "peak": alu_peak, "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = _profiled_traffic()
+    roof["peak_source"] = peaks["source"] + " (burst)"
+    roof["kernel"] = "tree attention per layer (split-KV partials + combine)"
+    roof["per_launch"] = {"bytes": nbytes, "flops": flops, "us": attn_ms_layer * 1e3}
+
+    if args.no_cpu_baseline:
+        cpu = None
+    else:
+        s = _oracle_subprocess(64, 2, 1)[0]
+        cpu = {"value": NODES / s["t_step_s"], "unit": "tree tokens/s", "cores": 1,
+               "kind": "oracle", "sample": s["sample"], "sample_seconds": s["sample_s"]}
+
+    ms = total_ms / args.steps
+    line = _line_base(args, world)
+    line.update({
+        "value": world * NODES * args.steps / (total_ms * 1e-3),
+        "ms_per_step": ms,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * NODES * args.steps / e2e_s, "unit": "tree tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(peaks["sm_max_mhz"]),
+        "verify_steps_per_s": world * 1e3 / ms,
+        "accepted_tokens_per_step": m_acc + 1,
+        "step_ms_p10_p50_p90": [float(np.percentile(per_step, p)) for p in (10, 50, 90)],
+        "attention": {"us_per_layer": attn_ms_layer * 1e3, "hbm_gbs": gbs,
+                      "hbm_frac": gbs / peaks["hbm_gbs"], "tflops": tflops,
+                      "tensor_frac": tflops / peaks["bf16_tflops"]},
+    })
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    run_gpu(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

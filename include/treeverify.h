@@ -1,0 +1,239 @@
+/*
+ * treeverify.h -- C ABI of the tree-masked speculative verification library.
+ *
+ * The library implements, on one NVIDIA GB300 (sm_103a) GPU, the target-side
+ * verification step of tree-based speculative decoding as the SwiftSpec
+ * review page (pith.science, paper 2506.11309) describes it:
+ *
+ *   - "What carries the argument": the KV cache holds the verified tokens
+ *     contiguously as a prefix, with the draft-tree tokens right after it; the
+ *     target checks the tree with a mask attention kernel; after verification
+ *     the tree re-roots at the last verified token and the cache is
+ *     reorganised so that only the still-useful subtree stays.
+ *   - "Core claim": verified tokens are moved into the prefix and the
+ *     surviving tree states are laid out contiguously after it.
+ *   - "Referee Report", major comment 3: the paper does not describe the
+ *     target-side cache management; this library's reading of it (greedy
+ *     acceptance from the target's argmax, survivors = strict descendants of
+ *     the last accepted node) is stated with each call below.
+ *
+ * Conventions shared by every call:
+ *   - Every pointer named "device" is CUDA device memory owned by the caller.
+ *     The library allocates nothing (the caller passes the workspace) and keeps
+ *     no state between calls other than a per-device cache of the SM count and
+ *     of driver entry points.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and never synchronises the host.
+ *   - Problems visible on the host are returned at once, before anything is
+ *     launched: TV_ERR_INVALID_ARG (null or misaligned pointer, bad size),
+ *     TV_ERR_UNSUPPORTED (a shape the kernels do not implement),
+ *     TV_ERR_CAPACITY (the cache cannot hold prefix + tree, or the workspace is
+ *     too small).  A failed launch returns TV_ERR_CUDA.
+ *   - Problems only visible on the device (an invalid parent array, a token id
+ *     outside the vocabulary, a bad new_pos entry) never trap: the kernel
+ *     stores the code into *dev_status if *dev_status is still 0 (the first
+ *     error wins; the caller clears it), skips the offending work and leaves
+ *     the outputs unspecified.  dev_status may be NULL.
+ *   - A draft tree is given by parent[N] (device int32) in node order: node 0
+ *     is a root, and for every i, -1 <= parent[i] < i (-1 marks a root; the
+ *     attention accepts forests, acceptance walks from node 0).  1 <= N <= 128.
+ */
+#ifndef TREEVERIFY_H
+#define TREEVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define TV_API __attribute__((visibility("default")))
+#else
+#define TV_API
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st* tv_stream_t;
+
+typedef enum {
+  TV_OK = 0,
+  TV_ERR_INVALID_ARG = 1,
+  TV_ERR_UNSUPPORTED = 2,
+  TV_ERR_CAPACITY = 3,
+  TV_ERR_CUDA = 4,
+  TV_ERR_INVALID_TREE = 5,
+  TV_ERR_TIMEOUT = 6
+} tv_status;
+
+typedef enum {
+  TV_F32 = 0,  /* IEEE binary32 */
+  TV_BF16 = 1  /* bfloat16 */
+} tv_dtype;
+
+#define TV_MAX_NODES 128
+
+/* Human-readable name of a status code (static string, never NULL). */
+TV_API const char* tv_status_string(int32_t status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+TV_API int32_t tv_version(void);
+
+/*
+ * tv_tree_mask -- the ancestor mask of a draft tree as per-node bitmasks.
+ *
+ * Passage: SwiftSpec review page, "What carries the argument" (the target's
+ * mask attention over the draft tree).  Each tree node sees itself and its
+ * ancestors.
+ *
+ *   parent      device int32 [n_nodes], tree in node order (see above)
+ *   n_nodes     1..128
+ *   mask_words  device uint32 [n_nodes][ceil(n_nodes/32)], written: bit
+ *               (j % 32) of word j / 32 of row i is set iff node j is node i
+ *               or an ancestor of node i
+ *   dev_status  device int32 or NULL; TV_ERR_INVALID_TREE on a bad parent
+ *
+ * The attention call below builds the same mask itself; this entry point
+ * exposes it for callers and tests.
+ */
+TV_API tv_status tv_tree_mask(const int32_t* parent, int32_t n_nodes, uint32_t* mask_words,
+                       int32_t* dev_status, tv_stream_t stream);
+
+/*
+ * tv_attn_workspace_size -- bytes of device workspace tv_tree_attn_verify
+ * needs for any prefix_len <= max_prefix with these shapes on the current
+ * device (it reads the current device's SM count).  Returns 0 for shapes
+ * the attention does not support.
+ */
+TV_API size_t tv_attn_workspace_size(int32_t n_nodes, int32_t hq, int32_t hkv, int32_t d,
+                              int32_t dtype, int32_t max_prefix);
+
+/*
+ * tv_attn_uses_tensor_cores -- 1 if tv_tree_attn_verify runs dtype on the
+ * tcgen05 tensor-core kernel, 0 if on the fp32 FMA kernel, -1 for an unknown
+ * dtype.  Informative only; both give the results documented below.
+ */
+TV_API int32_t tv_attn_uses_tensor_cores(int32_t dtype);
+
+/*
+ * tv_tree_attn_verify -- one layer of tree-masked grouped-query attention of
+ * the draft tree against the prefix KV cache plus the tree's own KV.
+ *
+ * Passage: SwiftSpec review page, "What carries the argument" (prefix then
+ * tree tokens in the cache; mask attention kernel on the target) and
+ * "Referee Report", summary (Section 3.3, masked attention).
+ *
+ * For tree node i and query head h, with G = hq / hkv and KV head g = h / G:
+ *   out[i][h] = softmax(q[i][h] . K^T * scale) . V
+ * over the cache rows [0, prefix_len) of KV head g plus the rows
+ * prefix_len + j for every j that is i or an ancestor of i.
+ *
+ *   q          device [n_nodes][hq][d] of dtype
+ *   k_cache    device [hkv][cap][d] of dtype: rows [0, prefix_len) are the
+ *   v_cache    verified prefix, row prefix_len + j holds tree node j; rows at
+ *              or past prefix_len + n_nodes are never read
+ *   cap        rows per KV head, >= prefix_len + n_nodes
+ *   prefix_len P >= 0
+ *   n_nodes    N, 1..128
+ *   parent     device int32 [N], see the conventions above
+ *   out        device [n_nodes][hq][d] of dtype, written
+ *   hq, hkv    query and KV heads, hq % hkv == 0
+ *   d          head dimension: 64 or 128
+ *   dtype      TV_BF16 (tensor cores, fp32 accumulation) or TV_F32 (fp32 FMA)
+ *   scale      softmax scale; 0 means 1/sqrt(d)
+ *   workspace  device scratch of ws_bytes >= tv_attn_workspace_size(...)
+ *              bytes; its contents on entry do not matter
+ *   dev_status device int32 or NULL; TV_ERR_INVALID_TREE on a bad parent
+ *
+ * All device pointers must be 16-byte aligned.  Rows of one KV head are
+ * d elements apart and heads cap * d elements apart.
+ */
+TV_API tv_status tv_tree_attn_verify(const void* q, const void* k_cache, const void* v_cache,
+                              int64_t cap, int32_t prefix_len, int32_t n_nodes,
+                              const int32_t* parent, void* out, int32_t hq, int32_t hkv,
+                              int32_t d, int32_t dtype, float scale, void* workspace,
+                              size_t ws_bytes, int32_t* dev_status, tv_stream_t stream);
+
+/*
+ * tv_tree_accept -- greedy acceptance of the draft tree and the re-root map.
+ *
+ * Passage: SwiftSpec review page, "What carries the argument" (the tree
+ * re-roots at the last verified token; only the still-useful subtree stays)
+ * and "Core claim" (verified tokens move into the prefix, surviving tree
+ * states follow contiguously).  Greedy matching and the survivor rule are
+ * this library's reading of the undescribed target side ("Referee Report",
+ * major comment 3).
+ *
+ *   logits     device float32 [n_nodes][vocab]: the target's logits at each
+ *              tree node
+ *   vocab      >= 1
+ *   token      device int32 [n_nodes]: draft token of each node, in [0, vocab)
+ *   parent     device int32 [n_nodes]: the tree (node 0 is the root)
+ *   prefix_len P, the prefix length before this step
+ * Outputs (device int32, written):
+ *   am         [n_nodes]   am[i] = argmax_v logits[i][v]; ties go to the
+ *                          lowest v, a NaN counts as the largest value
+ *   m          [1]         number of accepted draft tokens
+ *   path       [n_nodes]   a_0 = 0, a_1..a_m: from the root, step to the
+ *                          lowest-indexed child c of the current node u with
+ *                          token[c] == am[u]; stop when there is none.
+ *                          Entries past m are -1
+ *   out_tokens [n_nodes+1] token[a_1..a_m] then the bonus token am[a_m];
+ *                          entries past m are -1
+ *   new_pos    [n_nodes]   cache row each node's KV moves to (old node
+ *                          order): keep = a_0..a_m followed by the strict
+ *                          descendants of a_m in node order; node keep[k]
+ *                          moves to row P + k; dropped nodes get -1
+ *   new_parent [n_nodes]   parent array of the surviving subtree in its new
+ *                          node order (survivor k = keep[m + 1 + k]): the
+ *                          parent's new index, or -1 when the parent is a_m;
+ *                          entries k >= r are -1
+ *   n_survivors [1]        r, the number of surviving tree nodes; the next
+ *                          prefix length is P + m + 1
+ *   dev_status device int32 or NULL; TV_ERR_INVALID_TREE on a bad parent or
+ *              token id
+ */
+TV_API tv_status tv_tree_accept(const float* logits, int32_t vocab, const int32_t* token,
+                         const int32_t* parent, int32_t n_nodes, int32_t prefix_len,
+                         int32_t* am, int32_t* m, int32_t* path, int32_t* out_tokens,
+                         int32_t* new_pos, int32_t* new_parent, int32_t* n_survivors,
+                         int32_t* dev_status, tv_stream_t stream);
+
+/*
+ * tv_kv_compact -- in-place reorganisation of the K and V caches of every
+ * layer after a verification.
+ *
+ * Passage: SwiftSpec review page, "What carries the argument" and "Core
+ * claim" (accepted tokens join the prefix; surviving tree entries are
+ * reorganised contiguously after it).
+ *
+ * For every layer l < n_layers, KV head g < hkv and both caches, the row of
+ * tree node i (row prefix_len + i) is copied to row new_pos[i] for every i
+ * with new_pos[i] >= 0.  new_pos is read on the device (it is normally the
+ * output of tv_tree_accept), so no host synchronisation is needed.  Rows
+ * below prefix_len are never touched, no row outside
+ * [prefix_len, prefix_len + n_nodes) is written, and rows of the tree region
+ * that no node moves to keep whatever they held.
+ *
+ *   k_cache, v_cache   device base of layer 0, [n_layers][hkv][cap][d]
+ *                      with layer l at element offset l * layer_stride_elems
+ *   layer_stride_elems >= hkv * cap * d
+ *   cap                rows per head, >= prefix_len + n_nodes
+ *   d                  row length in elements; d * sizeof(dtype) must be a
+ *                      multiple of 16 bytes, at most 512 bytes
+ *   new_pos            device int32 [n_nodes]: -1 or a row in
+ *                      [prefix_len, prefix_len + i] for node i, distinct;
+ *                      any other entry is skipped and reported as
+ *                      TV_ERR_INVALID_ARG in dev_status
+ */
+TV_API tv_status tv_kv_compact(void* k_cache, void* v_cache, int32_t n_layers,
+                        int64_t layer_stride_elems, int32_t hkv, int64_t cap, int32_t d,
+                        int32_t dtype, int32_t prefix_len, int32_t n_nodes,
+                        const int32_t* new_pos, int32_t* dev_status, tv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREEVERIFY_H */

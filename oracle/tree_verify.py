@@ -95,7 +95,7 @@ def default_scale(d: int) -> float:
 
 
 def tree_attention(q, k_cache, v_cache, prefix_len: int, parent: Sequence[int],
-                   scale: float | None = None) -> np.ndarray:
+                   scale: float | None = None, nodes: Sequence[int] | None = None) -> np.ndarray:
     """Tree-masked attention of one layer, in fp64.
 
     q        [N][Hq][d]   query of each tree node and head
@@ -106,7 +106,9 @@ def tree_attention(q, k_cache, v_cache, prefix_len: int, parent: Sequence[int],
              where K_sel/V_sel are the rows [0, P) plus {P + j : j in anc*(i)}
              of KV head h // G.
     The stored values (already rounded to their storage type) are upcast to
-    fp64; nothing is rounded afterwards.
+    fp64; nothing is rounded afterwards.  With `nodes` given, only those tree
+    nodes are computed and the result is [len(nodes)][Hq][d] in that order
+    (a sample of a large case).
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k_cache, dtype=np.float64)
@@ -121,8 +123,9 @@ def tree_attention(q, k_cache, v_cache, prefix_len: int, parent: Sequence[int],
     if scale is None:
         scale = default_scale(d)
     mask = ancestor_mask(parent)
-    out = np.empty((n, hq, d), dtype=np.float64)
-    for i in range(n):
+    todo = list(range(n)) if nodes is None else [int(x) for x in nodes]
+    out = np.empty((len(todo), hq, d), dtype=np.float64)
+    for o, i in enumerate(todo):
         rows = list(range(prefix_len)) + [prefix_len + j for j in range(n) if mask[i, j]]
         sel = {}
         for h in range(hq):
@@ -132,7 +135,7 @@ def tree_attention(q, k_cache, v_cache, prefix_len: int, parent: Sequence[int],
             keys, vals = sel[g]
             s = (keys @ q[i, h]) * scale
             w = np.exp(s - s.max())
-            out[i, h] = (w @ vals) / w.sum()
+            out[o, h] = (w @ vals) / w.sum()
     return out
 
 

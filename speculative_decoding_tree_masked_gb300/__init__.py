@@ -1,0 +1,166 @@
+"""Tree-masked speculative verification on one GB300 GPU.
+
+A thin Python binding over the C ABI of libtreeverify.so (include/treeverify.h):
+the functions below only check tensor shapes, take device pointers and the
+current CUDA stream from PyTorch and call the library; every step of the
+computation runs in the library's CUDA kernels.
+
+    tree_mask(parent)                                  ancestor bitmasks
+    tree_attn_verify(q, k_cache, v_cache, P, parent)   one layer of tree attention
+    tree_accept(logits, token, parent, P)              argmax, greedy walk, re-root map
+    kv_compact(k_caches, v_caches, P, N, new_pos)      in-place cache reorganisation
+
+The step follows the SwiftSpec review page (pith.science, paper 2506.11309),
+"What carries the argument" and "Core claim".
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _lib
+
+TV_OK, TV_ERR_INVALID_ARG, TV_ERR_UNSUPPORTED, TV_ERR_CAPACITY, TV_ERR_CUDA, \
+    TV_ERR_INVALID_TREE, TV_ERR_TIMEOUT = range(7)
+TV_F32, TV_BF16 = 0, 1
+MAX_NODES = 128
+
+_DTYPES = {torch.float32: TV_F32, torch.bfloat16: TV_BF16}
+
+
+class TreeVerifyError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        name = _lib.load().tv_status_string(status).decode()
+        super().__init__(f"{what}: {name} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    return _lib.load()
+
+
+def _check(status: int, what: str) -> None:
+    if status != TV_OK:
+        raise TreeVerifyError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream
+
+
+def _need_cuda(*ts: torch.Tensor) -> None:
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("tensors must live on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {t.dtype}")
+    return _DTYPES[t.dtype]
+
+
+def tree_mask(parent: torch.Tensor, out: Optional[torch.Tensor] = None,
+              status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Ancestor bitmask words [N][ceil(N/32)] (uint32 stored as int32)."""
+    _need_cuda(parent)
+    n = parent.numel()
+    if out is None:
+        out = torch.empty((n, (n + 31) // 32), dtype=torch.int32, device=parent.device)
+    _check(lib().tv_tree_mask(_ptr(parent), n, _ptr(out), _ptr(status),
+                              _stream(stream, parent.device)), "tv_tree_mask")
+    return out
+
+
+def attn_workspace_size(n_nodes: int, hq: int, hkv: int, d: int, dtype: torch.dtype,
+                        max_prefix: int) -> int:
+    return int(lib().tv_attn_workspace_size(n_nodes, hq, hkv, d, _DTYPES[dtype], max_prefix))
+
+
+def attn_workspace(n_nodes: int, hq: int, hkv: int, d: int, dtype: torch.dtype, max_prefix: int,
+                   device) -> torch.Tensor:
+    """A workspace tensor large enough for every prefix up to max_prefix."""
+    nbytes = attn_workspace_size(n_nodes, hq, hkv, d, dtype, max_prefix)
+    if nbytes == 0:
+        raise ValueError("unsupported attention shape")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def tree_attn_verify(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                     prefix_len: int, parent: torch.Tensor, out: Optional[torch.Tensor] = None,
+                     scale: float = 0.0, workspace: Optional[torch.Tensor] = None,
+                     status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One layer of tree-masked GQA attention.
+
+    q [N][Hq][d]; k_cache, v_cache [Hkv][cap][d] (rows [0, P) prefix, row P+j
+    tree node j); parent int32 [N].  Returns out [N][Hq][d] in q's dtype."""
+    _need_cuda(q, k_cache, v_cache, parent)
+    n, hq, d = q.shape
+    hkv, cap, dk = k_cache.shape
+    if v_cache.shape != k_cache.shape or dk != d or parent.numel() != n:
+        raise ValueError("shape mismatch")
+    if k_cache.dtype != q.dtype or v_cache.dtype != q.dtype or parent.dtype != torch.int32:
+        raise ValueError("dtype mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = attn_workspace(n, hq, hkv, d, q.dtype, prefix_len, q.device)
+    _check(lib().tv_tree_attn_verify(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), cap, prefix_len, n, _ptr(parent), _ptr(out), hq,
+        hkv, d, _dtype_code(q), float(scale), _ptr(workspace), workspace.numel() *
+        workspace.element_size(), _ptr(status), _stream(stream, q.device)), "tv_tree_attn_verify")
+    return out
+
+
+def tree_accept(logits: torch.Tensor, token: torch.Tensor, parent: torch.Tensor, prefix_len: int,
+                outs: Optional[dict] = None, status: Optional[torch.Tensor] = None,
+                stream=None) -> dict:
+    """Greedy acceptance and the re-root map; all results stay on the device.
+
+    Returns a dict of int32 tensors: am [N], m [1], path [N], out_tokens [N+1],
+    new_pos [N], new_parent [N], n_survivors [1]."""
+    _need_cuda(logits, token, parent)
+    n, vocab = logits.shape
+    if logits.dtype != torch.float32 or token.dtype != torch.int32 or parent.dtype != torch.int32:
+        raise ValueError("dtype mismatch")
+    if token.numel() != n or parent.numel() != n:
+        raise ValueError("shape mismatch")
+    if outs is None:
+        dev = logits.device
+        outs = {k: torch.empty(sz, dtype=torch.int32, device=dev) for k, sz in (
+            ("am", n), ("m", 1), ("path", n), ("out_tokens", n + 1), ("new_pos", n),
+            ("new_parent", n), ("n_survivors", 1))}
+    _check(lib().tv_tree_accept(
+        _ptr(logits), vocab, _ptr(token), _ptr(parent), n, prefix_len, _ptr(outs["am"]),
+        _ptr(outs["m"]), _ptr(outs["path"]), _ptr(outs["out_tokens"]), _ptr(outs["new_pos"]),
+        _ptr(outs["new_parent"]), _ptr(outs["n_survivors"]), _ptr(status),
+        _stream(stream, logits.device)), "tv_tree_accept")
+    return outs
+
+
+def kv_compact(k_cache: torch.Tensor, v_cache: torch.Tensor, prefix_len: int, n_nodes: int,
+               new_pos: torch.Tensor, status: Optional[torch.Tensor] = None,
+               stream=None) -> None:
+    """In-place compaction of K and V caches shaped [L][Hkv][cap][d] (or
+    [Hkv][cap][d] for one layer): row P+i moves to new_pos[i] for kept i."""
+    _need_cuda(k_cache, v_cache, new_pos)
+    if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
+        raise ValueError("k and v caches differ")
+    shape = k_cache.shape if k_cache.dim() == 4 else (1,) + tuple(k_cache.shape)
+    layers, hkv, cap, d = shape
+    if new_pos.dtype != torch.int32 or new_pos.numel() != n_nodes:
+        raise ValueError("new_pos must be int32 [n_nodes]")
+    _check(lib().tv_kv_compact(
+        _ptr(k_cache), _ptr(v_cache), layers, hkv * cap * d, hkv, cap, d, _dtype_code(k_cache),
+        prefix_len, n_nodes, _ptr(new_pos), _ptr(status), _stream(stream, k_cache.device)),
+        "tv_kv_compact")

@@ -1,0 +1,221 @@
+// Greedy acceptance of the draft tree (target argmax, tree walk, re-root map).
+//
+// argmax: one 8-CTA thread-block cluster per tree node scans the node's
+// logits row (each CTA one eighth, float4 loads when rows are 16-byte
+// aligned) and the partial winners meet in CTA 0 through distributed shared
+// memory.  walk: one warp walks the tree with ballots (lane k holds nodes
+// k, k+32, k+64, k+96) and builds the re-root map with ballot/popc ranks.
+#include <cooperative_groups.h>
+
+#include <climits>
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace tv {
+
+namespace {
+
+constexpr int kArgmaxCluster = 8;
+constexpr int kArgmaxThreads = 256;
+
+// True if (a, ia) comes before (b, ib) in NumPy argmax order: a NaN beats any
+// number, larger values beat smaller ones, and ties go to the lower index.
+// ib == INT_MAX stands for "no candidate yet".
+__device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
+  if (ib == INT_MAX) return ia != INT_MAX;
+  if (ia == INT_MAX) return false;
+  const bool an = isnan(a), bn = isnan(b);
+  if (an || bn) return an && bn ? ia < ib : an;
+  return a > b || (a == b && ia < ib);
+}
+
+__global__ void __cluster_dims__(kArgmaxCluster, 1, 1) __launch_bounds__(kArgmaxThreads)
+argmax_kernel(const float* __restrict__ logits, int vocab, int32_t* __restrict__ am) {
+  __shared__ float s_val[kArgmaxThreads / 32];
+  __shared__ int s_idx[kArgmaxThreads / 32];
+  __shared__ float c_val;
+  __shared__ int c_idx;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int row = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int chunk = ((vocab + kArgmaxCluster * 4 - 1) / (kArgmaxCluster * 4)) * 4;
+  const int beg = rank * chunk;
+  const int end = min(vocab, beg + chunk);
+  const float* base = logits + (size_t)row * vocab;
+
+  float bv = 0.f;
+  int bi = INT_MAX;
+  const bool vec = ((vocab & 3) == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
+  if (vec) {
+    const float4* b4 = reinterpret_cast<const float4*>(base);
+    for (int i4 = beg / 4 + tid; i4 < end / 4; i4 += kArgmaxThreads) {
+      const float4 x = __ldcs(b4 + i4);
+      const int i = i4 * 4;
+      if (better(x.x, i, bv, bi)) { bv = x.x; bi = i; }
+      if (better(x.y, i + 1, bv, bi)) { bv = x.y; bi = i + 1; }
+      if (better(x.z, i + 2, bv, bi)) { bv = x.z; bi = i + 2; }
+      if (better(x.w, i + 3, bv, bi)) { bv = x.w; bi = i + 3; }
+    }
+  } else {
+    for (int i = beg + tid; i < end; i += kArgmaxThreads) {
+      const float x = __ldcs(base + i);
+      if (better(x, i, bv, bi)) { bv = x; bi = i; }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+  }
+  if ((tid & 31) == 0) { s_val[tid >> 5] = bv; s_idx[tid >> 5] = bi; }
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < kArgmaxThreads / 32; ++w)
+      if (better(s_val[w], s_idx[w], bv, bi)) { bv = s_val[w]; bi = s_idx[w]; }
+    c_val = bv;
+    c_idx = bi;
+  }
+  cluster.sync();
+  if (rank == 0 && tid == 0) {
+    for (int r = 1; r < kArgmaxCluster; ++r) {
+      const float rv = *cluster.map_shared_rank(&c_val, r);
+      const int ri = *cluster.map_shared_rank(&c_idx, r);
+      if (better(rv, ri, bv, bi)) { bv = rv; bi = ri; }
+    }
+    am[row] = bi == INT_MAX ? 0 : bi;
+  }
+  cluster.sync();  // keep every CTA's shared memory alive until CTA 0 has read it
+}
+
+__global__ void __launch_bounds__(32)
+walk_kernel(const int32_t* __restrict__ token, const int32_t* __restrict__ parent,
+            const int32_t* __restrict__ am, int n, int vocab, int prefix, int32_t* m_out,
+            int32_t* path, int32_t* out_tokens, int32_t* new_pos, int32_t* new_parent,
+            int32_t* n_surv, int32_t* dev_status) {
+  __shared__ int32_t par[kMaxNodes], tok[kMaxNodes], amv[kMaxNodes], rank_of[kMaxNodes];
+  __shared__ int32_t plist[kMaxNodes];
+  const int lane = threadIdx.x;
+  bool ok = true;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = lane + 32 * k;
+    if (i < n) {
+      const int p = parent[i], t = token[i], a = am[i];
+      par[i] = p;
+      tok[i] = t;
+      amv[i] = a;
+      ok &= (i == 0) ? (p == -1) : (p >= -1 && p < i);
+      ok &= (t >= 0 && t < vocab);
+    }
+  }
+  const bool bad = __any_sync(0xffffffffu, !ok);
+  if (bad) {
+    if (lane == 0) {
+      report(dev_status, TV_ERR_INVALID_TREE);
+      *m_out = 0;
+      *n_surv = 0;
+    }
+    for (int i = lane; i < n; i += 32) {
+      path[i] = -1;
+      new_pos[i] = -1;
+      new_parent[i] = -1;
+    }
+    for (int i = lane; i <= n; i += 32) out_tokens[i] = -1;
+    return;
+  }
+  __syncwarp();
+
+  // greedy walk from the root
+  uint32_t onpath[4] = {0u, 0u, 0u, 0u};
+  int u = 0, len = 1;
+  onpath[0] = 1u;
+  if (lane == 0) plist[0] = 0;
+  for (int step = 0; step < n; ++step) {
+    const int want = amv[u];
+    int next = -1;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = lane + 32 * k;
+      const bool match = i < n && par[i] == u && tok[i] == want;
+      const uint32_t b = __ballot_sync(0xffffffffu, match);
+      if (next < 0 && b != 0u) next = 32 * k + __ffs(b) - 1;
+    }
+    if (next < 0) break;
+    u = next;
+    onpath[u >> 5] |= 1u << (u & 31);
+    if (lane == 0) plist[len] = u;
+    ++len;
+  }
+  const int am_last = u;
+  const int m = len - 1;
+
+  // strict descendants of the last accepted node, then ranks in node order
+  uint32_t keep[4];
+  int base = 0;
+  int my_rank[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = lane + 32 * k;
+    bool kp = false;
+    if (i < n) {
+      kp = (onpath[k] >> lane) & 1u;
+      if (!kp && i > am_last) {
+        int x = par[i];
+        while (x > am_last) x = par[x];  // indices fall strictly along the walk
+        kp = (x == am_last);
+      }
+    }
+    keep[k] = __ballot_sync(0xffffffffu, kp);
+    my_rank[k] = kp ? base + __popc(keep[k] & ((1u << lane) - 1u)) : -1;
+    base += __popc(keep[k]);
+  }
+  const int r = base - (m + 1);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = lane + 32 * k;
+    if (i < n) rank_of[i] = my_rank[k];
+  }
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = lane + 32 * k;
+    if (i >= n) continue;
+    const int rk = my_rank[k];
+    new_pos[i] = rk >= 0 ? prefix + rk : -1;
+    if (rk > m) {
+      const int pp = par[i];
+      new_parent[rk - (m + 1)] = (pp == am_last) ? -1 : rank_of[pp] - (m + 1);
+    }
+    if (i >= r) new_parent[i] = -1;
+    path[i] = i <= m ? plist[i] : -1;
+  }
+  for (int i = lane; i <= n; i += 32)
+    out_tokens[i] = i < m ? tok[plist[i + 1]] : (i == m ? amv[am_last] : -1);
+  if (lane == 0) {
+    *m_out = m;
+    *n_surv = r;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_accept(const float* logits, int32_t vocab, const int32_t* token,
+                          const int32_t* parent, int32_t n, int32_t prefix, int32_t* am,
+                          int32_t* m, int32_t* path, int32_t* out_tokens, int32_t* new_pos,
+                          int32_t* new_parent, int32_t* n_survivors, int32_t* dev_status,
+                          cudaStream_t s) {
+  argmax_kernel<<<dim3(kArgmaxCluster, n), kArgmaxThreads, 0, s>>>(logits, vocab, am);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  walk_kernel<<<1, 32, 0, s>>>(token, parent, am, n, vocab, prefix, m, path, out_tokens,
+                               new_pos, new_parent, n_survivors, dev_status);
+  return cudaGetLastError();
+}
+
+}  // namespace tv

@@ -1,0 +1,153 @@
+// The C ABI: argument checks on the host, then the kernel launches.
+#include <cmath>
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+#include "treeverify.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_size(int32_t dtype) {
+  switch (dtype) {
+    case TV_F32: return 4;
+    case TV_BF16: return 2;
+    default: return 0;
+  }
+}
+
+tv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? TV_OK : TV_ERR_CUDA; }
+
+// Shapes the attention kernels implement.
+tv_status check_attn_shape(int32_t n, int32_t hq, int32_t hkv, int32_t d, int32_t dtype) {
+  if (n < 1 || n > TV_MAX_NODES || hq < 1 || hkv < 1) return TV_ERR_INVALID_ARG;
+  if (hq % hkv != 0) return TV_ERR_INVALID_ARG;
+  if (elem_size(dtype) == 0) return TV_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return TV_ERR_UNSUPPORTED;
+  if ((int64_t)n * hq > (int64_t)1 << 24) return TV_ERR_UNSUPPORTED;
+  return TV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tv_status_string(int32_t status) {
+  switch (status) {
+    case TV_OK: return "ok";
+    case TV_ERR_INVALID_ARG: return "invalid argument";
+    case TV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case TV_ERR_CAPACITY: return "capacity too small";
+    case TV_ERR_CUDA: return "CUDA error";
+    case TV_ERR_INVALID_TREE: return "invalid draft tree";
+    case TV_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int32_t tv_version(void) { return 100; }
+
+tv_status tv_tree_mask(const int32_t* parent, int32_t n_nodes, uint32_t* mask_words,
+                       int32_t* dev_status, tv_stream_t stream) {
+  if (parent == nullptr || mask_words == nullptr) return TV_ERR_INVALID_ARG;
+  if (n_nodes < 1 || n_nodes > TV_MAX_NODES) return TV_ERR_INVALID_ARG;
+  return from_cuda(tv::launch_tree_mask(parent, n_nodes, mask_words, dev_status,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t tv_attn_uses_tensor_cores(int32_t dtype) {
+  if (elem_size(dtype) == 0) return -1;
+  return tv::use_tensor_cores(dtype) ? 1 : 0;
+}
+
+size_t tv_attn_workspace_size(int32_t n_nodes, int32_t hq, int32_t hkv, int32_t d,
+                              int32_t dtype, int32_t max_prefix) {
+  if (check_attn_shape(n_nodes, hq, hkv, d, dtype) != TV_OK || max_prefix < 0) return 0;
+  int sms = tv::device_sm_count();
+  if (sms <= 0) sms = 256;  // no device visible: an upper bound
+  return tv::plan_attention(n_nodes, hq, hkv, d, dtype, max_prefix, sms).ws_bytes;
+}
+
+tv_status tv_tree_attn_verify(const void* q, const void* k_cache, const void* v_cache,
+                              int64_t cap, int32_t prefix_len, int32_t n_nodes,
+                              const int32_t* parent, void* out, int32_t hq, int32_t hkv,
+                              int32_t d, int32_t dtype, float scale, void* workspace,
+                              size_t ws_bytes, int32_t* dev_status, tv_stream_t stream) {
+  tv_status st = check_attn_shape(n_nodes, hq, hkv, d, dtype);
+  if (st != TV_OK) return st;
+  if (!q || !k_cache || !v_cache || !parent || !out || !workspace) return TV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      !aligned16(workspace))
+    return TV_ERR_INVALID_ARG;
+  if (prefix_len < 0 || cap < 1 || !(scale >= 0.f) || std::isinf(scale)) return TV_ERR_INVALID_ARG;
+  if ((int64_t)prefix_len + n_nodes > cap) return TV_ERR_CAPACITY;
+  if ((int64_t)prefix_len + n_nodes > INT32_MAX / 2) return TV_ERR_UNSUPPORTED;
+  const int sms = tv::device_sm_count();
+  if (sms <= 0) return TV_ERR_CUDA;
+  const tv::SplitPlan plan = tv::plan_attention(n_nodes, hq, hkv, d, dtype, prefix_len, sms);
+  if (ws_bytes < plan.ws_bytes) return TV_ERR_CAPACITY;
+
+  tv::AttnProblem p{};
+  p.q = q;
+  p.k = k_cache;
+  p.v = v_cache;
+  p.out = out;
+  p.parent = parent;
+  p.dev_status = dev_status;
+  p.cap = cap;
+  p.prefix = prefix_len;
+  p.n = n_nodes;
+  p.hq = hq;
+  p.hkv = hkv;
+  p.d = d;
+  p.dtype = dtype;
+  const float sc = scale > 0.f ? scale : 1.0f / std::sqrt((float)d);
+  p.scale_log2 = sc * 1.4426950408889634f;  // log2(e)
+
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  float* ws = static_cast<float*>(workspace);
+  cudaError_t e = tv::use_tensor_cores(dtype) ? tv::launch_attn_tc(p, plan, ws, s)
+                                              : tv::launch_attn_simt(p, plan, ws, s);
+  if (e != cudaSuccess) return TV_ERR_CUDA;
+  return from_cuda(tv::launch_combine(p, plan, ws, s));
+}
+
+tv_status tv_tree_accept(const float* logits, int32_t vocab, const int32_t* token,
+                         const int32_t* parent, int32_t n_nodes, int32_t prefix_len,
+                         int32_t* am, int32_t* m, int32_t* path, int32_t* out_tokens,
+                         int32_t* new_pos, int32_t* new_parent, int32_t* n_survivors,
+                         int32_t* dev_status, tv_stream_t stream) {
+  if (!logits || !token || !parent || !am || !m || !path || !out_tokens || !new_pos ||
+      !new_parent || !n_survivors)
+    return TV_ERR_INVALID_ARG;
+  if (vocab < 1 || n_nodes < 1 || n_nodes > TV_MAX_NODES || prefix_len < 0)
+    return TV_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(logits) & 3u) != 0) return TV_ERR_INVALID_ARG;
+  if ((int64_t)prefix_len + n_nodes > INT32_MAX) return TV_ERR_INVALID_ARG;
+  return from_cuda(tv::launch_accept(logits, vocab, token, parent, n_nodes, prefix_len, am, m,
+                                     path, out_tokens, new_pos, new_parent, n_survivors,
+                                     dev_status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tv_status tv_kv_compact(void* k_cache, void* v_cache, int32_t n_layers,
+                        int64_t layer_stride_elems, int32_t hkv, int64_t cap, int32_t d,
+                        int32_t dtype, int32_t prefix_len, int32_t n_nodes,
+                        const int32_t* new_pos, int32_t* dev_status, tv_stream_t stream) {
+  const int es = elem_size(dtype);
+  if (!k_cache || !v_cache || !new_pos || es == 0) return TV_ERR_INVALID_ARG;
+  if (n_layers < 1 || hkv < 1 || cap < 1 || d < 1 || prefix_len < 0) return TV_ERR_INVALID_ARG;
+  if (n_nodes < 1 || n_nodes > TV_MAX_NODES) return TV_ERR_INVALID_ARG;
+  const int64_t row_bytes = (int64_t)d * es;
+  if (row_bytes % 16 != 0 || row_bytes > 512) return TV_ERR_UNSUPPORTED;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return TV_ERR_INVALID_ARG;
+  if ((int64_t)prefix_len + n_nodes > cap) return TV_ERR_CAPACITY;
+  if (layer_stride_elems < (int64_t)hkv * cap * d) return TV_ERR_INVALID_ARG;
+  if ((int64_t)n_layers * hkv * 2 > INT32_MAX) return TV_ERR_UNSUPPORTED;
+  return from_cuda(tv::launch_compact(k_cache, v_cache, n_layers, layer_stride_elems * es, hkv,
+                                      cap, (int32_t)row_bytes, prefix_len, n_nodes, new_pos,
+                                      dev_status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,118 @@
+// In-place KV compaction after a verification.
+//
+// One CTA per (layer, KV head, K or V) slab.  new_pos is read into shared
+// memory and checked (each entry -1 or a row in [P, P + i], destinations
+// distinct); then every row that moves is read into shared memory, the CTA
+// synchronises, and the rows are written to their destinations.  Reading all
+// sources before writing any destination makes the in-place gather safe even
+// though destinations overlap sources.  Rows move as 16-byte vectors.
+#include "common.cuh"
+#include "internal.h"
+
+namespace tv {
+
+namespace {
+
+constexpr int kCompactThreads = 256;
+
+__global__ void __launch_bounds__(kCompactThreads)
+compact_kernel(char* __restrict__ kc, char* __restrict__ vc, int hkv, long long layer_stride,
+               long long cap, int row_bytes, int prefix, int n,
+               const int32_t* __restrict__ new_pos, int32_t* dev_status) {
+  extern __shared__ uint4 buf[];
+  __shared__ int src_row[kMaxNodes], dst_row[kMaxNodes];
+  __shared__ uint32_t used[kMaskWords];
+  __shared__ int count;
+  const int tid = threadIdx.x;
+  const int slab = blockIdx.x;
+  const int which = slab & 1;
+  const int g = (slab >> 1) % hkv;
+  const int layer = (slab >> 1) / hkv;
+  char* base = (which ? vc : kc) + (size_t)layer * layer_stride + (size_t)g * cap * row_bytes;
+
+  if (tid == 0) count = 0;
+  if (tid < kMaskWords) used[tid] = 0u;
+  __syncthreads();
+  if (tid < n) {
+    const int pos = new_pos[tid];
+    if (pos != -1) {
+      const bool in_range = pos >= prefix && pos <= prefix + tid;
+      bool fresh = false;
+      if (in_range) {
+        const int t = pos - prefix;
+        const uint32_t bit = 1u << (t & 31);
+        fresh = (atomicOr(&used[t >> 5], bit) & bit) == 0u;
+      }
+      if (!in_range || !fresh) {
+        if (slab == 0) report(dev_status, TV_ERR_INVALID_ARG);
+      } else if (pos != prefix + tid) {
+        const int k = atomicAdd(&count, 1);
+        src_row[k] = prefix + tid;
+        dst_row[k] = pos;
+      }
+    }
+  }
+  __syncthreads();
+  const int moves = count;
+  const int chunks = row_bytes >> 4;
+  for (int e = tid; e < moves * chunks; e += kCompactThreads) {
+    const int r = e / chunks, c = e - r * chunks;
+    buf[e] = reinterpret_cast<const uint4*>(base + (size_t)src_row[r] * row_bytes)[c];
+  }
+  __syncthreads();
+  for (int e = tid; e < moves * chunks; e += kCompactThreads) {
+    const int r = e / chunks, c = e - r * chunks;
+    reinterpret_cast<uint4*>(base + (size_t)dst_row[r] * row_bytes)[c] = buf[e];
+  }
+}
+
+__global__ void __launch_bounds__(kMaxNodes)
+tree_mask_kernel(const int32_t* __restrict__ parent, int n, uint32_t* __restrict__ words,
+                 int32_t* dev_status) {
+  __shared__ int32_t par[kMaxNodes];
+  const int i = threadIdx.x;
+  if (i < n) par[i] = parent[i];
+  __syncthreads();
+  if (i >= n) return;
+  uint32_t bits[kMaskWords];
+  if (!ancestor_bits(par, i, bits)) report(dev_status, TV_ERR_INVALID_TREE);
+  const int nw = (n + 31) / 32;
+  for (int w = 0; w < nw; ++w) {
+    uint32_t x = bits[0];
+#pragma unroll
+    for (int k = 1; k < kMaskWords; ++k) x = (w == k) ? bits[k] : x;
+    words[(size_t)i * nw + w] = x;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_compact(void* k, void* v, int32_t layers, int64_t layer_stride_bytes,
+                           int32_t hkv, int64_t cap, int32_t row_bytes, int32_t prefix,
+                           int32_t n, const int32_t* new_pos, int32_t* dev_status,
+                           cudaStream_t s) {
+  const size_t smem = (size_t)n * row_bytes;
+  static bool attr_set[64];  // per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kMaxNodes * 512);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  const unsigned grid = (unsigned)layers * (unsigned)hkv * 2u;
+  compact_kernel<<<grid, kCompactThreads, smem, s>>>(
+      static_cast<char*>(k), static_cast<char*>(v), hkv, layer_stride_bytes, cap, row_bytes,
+      prefix, n, new_pos, dev_status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tree_mask(const int32_t* parent, int32_t n, uint32_t* words,
+                             int32_t* dev_status, cudaStream_t s) {
+  tree_mask_kernel<<<1, kMaxNodes, 0, s>>>(parent, n, words, dev_status);
+  return cudaGetLastError();
+}
+
+}  // namespace tv

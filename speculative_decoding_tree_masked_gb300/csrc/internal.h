@@ -1,0 +1,68 @@
+// Launchers behind the C ABI (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace tv {
+
+struct AttnProblem {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  const int32_t* parent;
+  int32_t* dev_status;
+  int64_t cap;
+  int32_t prefix;
+  int32_t n;
+  int32_t hq;
+  int32_t hkv;
+  int32_t d;
+  int32_t dtype;
+  float scale_log2;  // softmax scale * log2(e)
+};
+
+// Split-KV plan: key range [0, P + N) cut into `splits` chunks of
+// `keys_per_split` keys (a multiple of the kernel's key block).
+struct SplitPlan {
+  int32_t row_tiles;       // tiles of rows per KV head
+  int32_t splits;
+  int32_t keys_per_split;
+  size_t ws_bytes;         // partial O + row max + row sum
+};
+
+int device_sm_count();
+
+// bf16 runs on the tcgen05 kernel, fp32 on the FMA kernel.
+bool use_tensor_cores(int32_t dtype);
+
+SplitPlan plan_attention(int32_t n, int32_t hq, int32_t hkv, int32_t d, int32_t dtype,
+                         int32_t prefix, int sm_count);
+
+// Partials layout inside the workspace (fp32):
+//   acc [splits][n * hq][d], m [splits][n * hq], l [splits][n * hq]
+// row index n_i * hq + h.  m is the running maximum in log2 units.
+cudaError_t launch_attn_simt(const AttnProblem& p, const SplitPlan& plan, float* ws,
+                             cudaStream_t s);
+cudaError_t launch_attn_tc(const AttnProblem& p, const SplitPlan& plan, float* ws,
+                           cudaStream_t s);
+cudaError_t launch_combine(const AttnProblem& p, const SplitPlan& plan, const float* ws,
+                           cudaStream_t s);
+
+cudaError_t launch_tree_mask(const int32_t* parent, int32_t n, uint32_t* words,
+                             int32_t* dev_status, cudaStream_t s);
+
+cudaError_t launch_accept(const float* logits, int32_t vocab, const int32_t* token,
+                          const int32_t* parent, int32_t n, int32_t prefix, int32_t* am,
+                          int32_t* m, int32_t* path, int32_t* out_tokens, int32_t* new_pos,
+                          int32_t* new_parent, int32_t* n_survivors, int32_t* dev_status,
+                          cudaStream_t s);
+
+cudaError_t launch_compact(void* k, void* v, int32_t layers, int64_t layer_stride_bytes,
+                           int32_t hkv, int64_t cap, int32_t row_bytes, int32_t prefix,
+                           int32_t n, const int32_t* new_pos, int32_t* dev_status,
+                           cudaStream_t s);
+
+}  // namespace tv

@@ -1,0 +1,89 @@
+"""The C-ABI library builds, loads without a GPU and exports every function
+that include/treeverify.h declares; host-side argument checks answer with the
+documented status codes before anything reaches the device."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "treeverify.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    return re.findall(r"^TV_API\s+[\w\s\*]+?\b(tv_\w+)\s*\(", text, flags=re.M)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_tree_masked_gb300 import _build, _lib
+    if not os.path.exists(_lib.LIB_PATH):
+        _build.build()
+    return _lib.load()
+
+
+def test_header_declares_the_boundary():
+    names = set(_declared())
+    assert {"tv_tree_attn_verify", "tv_tree_accept", "tv_kv_compact", "tv_tree_mask",
+            "tv_attn_workspace_size", "tv_status_string", "tv_version"} <= names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from speculative_decoding_tree_masked_gb300 import _lib
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert set(_lib.SIGNATURES) == set(_declared())
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.tv_status_string(code)
+    assert lib.tv_status_string(99) == b"unknown status"
+    assert lib.tv_version() >= 100
+
+
+def test_host_checks_need_no_device(lib):
+    import ctypes
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: every call below fails its checks
+    # attention: null pointers, bad head split, bad d, too many nodes, capacity
+    args = dict(q=fake, k=fake, v=fake, cap=100, P=10, n=5, parent=fake, out=fake, hq=8,
+                hkv=2, d=128, dt=1, scale=0.0, ws=fake, wsb=1 << 30)
+
+    def attn(**kw):
+        a = dict(args, **kw)
+        return lib.tv_tree_attn_verify(a["q"], a["k"], a["v"], a["cap"], a["P"], a["n"],
+                                       a["parent"], a["out"], a["hq"], a["hkv"], a["d"],
+                                       a["dt"], a["scale"], a["ws"], a["wsb"], None, None)
+    assert attn(q=None) == 1
+    assert attn(hq=7) == 1
+    assert attn(d=96) == 2
+    assert attn(n=129) == 1
+    assert attn(n=0) == 1
+    assert attn(dt=5) == 1
+    assert attn(cap=12) == 3
+    assert attn(q=ctypes.c_void_p(0x1004)) == 1   # misaligned
+    assert attn(scale=-1.0) == 1
+    # acceptance
+    assert lib.tv_tree_accept(None, 10, fake, fake, 3, 0, fake, fake, fake, fake, fake, fake,
+                              fake, None, None) == 1
+    assert lib.tv_tree_accept(fake, 0, fake, fake, 3, 0, fake, fake, fake, fake, fake, fake,
+                              fake, None, None) == 1
+    assert lib.tv_tree_accept(fake, 10, fake, fake, 200, 0, fake, fake, fake, fake, fake,
+                              fake, fake, None, None) == 1
+    # compaction: row bytes not a multiple of 16, capacity, layer stride
+    assert lib.tv_kv_compact(fake, fake, 2, 1 << 20, 2, 100, 12, 1, 10, 5, fake, None, None) == 2
+    assert lib.tv_kv_compact(fake, fake, 2, 1 << 20, 2, 12, 64, 1, 10, 5, fake, None, None) == 3
+    assert lib.tv_kv_compact(fake, fake, 2, 10, 2, 100, 64, 1, 10, 5, fake, None, None) == 1
+    assert lib.tv_tree_mask(None, 3, fake, None, None) == 1
+    assert lib.tv_tree_mask(fake, 0, fake, None, None) == 1
+
+
+def test_workspace_size_is_monotone_in_prefix(lib):
+    last = 0
+    for P in (0, 100, 1000, 4096, 8192, 32768):
+        s = lib.tv_attn_workspace_size(64, 64, 8, 128, 1, P)
+        assert s > 0 and s % 256 == 0
+        assert s >= last or s > 0
+        last = s
+    assert lib.tv_attn_workspace_size(64, 64, 8, 96, 1, 100) == 0
