@@ -91,9 +91,9 @@ def attn_workspace(n_nodes: int, hq: int, hkv: int, d: int, dtype: torch.dtype, 
                    device) -> torch.Tensor:
     """A workspace tensor large enough for every prefix up to max_prefix."""
     nbytes = attn_workspace_size(n_nodes, hq, hkv, d, dtype, max_prefix)
-    if nbytes == 0:
-        raise ValueError("unsupported attention shape")
-    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+    # 0 means the library does not take this shape; a token buffer lets the
+    # call itself report why
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
 def tree_attn_verify(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

@@ -90,13 +90,14 @@ def test_full_verify_step_all_layers():
 def test_reroot_preserves_survivor_attention_on_gpu(seed):
     rng = np.random.default_rng(seed)
     n, P, hq, hkv, d = 64, 300, 8, 2, 128
-    parent = synth.random_parent_tree(rng, n, max_depth=10)
-    token = rng.integers(0, 2, size=n).astype(np.int32)
-    logits = rng.standard_normal((n, 2)).astype(np.float32)
-    want = oracle.tree_accept(logits, token, parent, P)
-    m, r = want["m"], want["n_survivors"]
-    if r == 0:
-        pytest.skip("no survivors for this draw")
+    while True:  # draw until some subtree survives
+        parent = synth.random_parent_tree(rng, n, max_depth=10)
+        token = rng.integers(0, 2, size=n).astype(np.int32)
+        logits = rng.standard_normal((n, 2)).astype(np.float32)
+        want = oracle.tree_accept(logits, token, parent, P)
+        m, r = want["m"], want["n_survivors"]
+        if r > 0:
+            break
     f = lambda *s: torch.from_numpy(rng.standard_normal(s, dtype=np.float32)).to(torch.bfloat16)
     q, k, v = f(n, hq, d), f(hkv, P + n, d), f(hkv, P + n, d)
     kd, vd = k.to(DEV), v.to(DEV)
