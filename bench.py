@@ -340,6 +340,8 @@ def run_gpu(args, rank, world, local_rank):
              for k in ("m", "out_tokens", "new_pos", "n_survivors")}
     g_e2e = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
+        for dst, src in ((q_d, q_h), (lg_d, lg_h), (tk_d, tk_h), (pr_d, pr_h)):
+            dst.copy_(src, non_blocking=True)
         step(q_d, lg_d, tk_d, pr_d)
     torch.cuda.synchronize()
     with torch.cuda.graph(g_e2e, stream=stream):
