@@ -108,9 +108,10 @@ tv_status tv_tree_attn_verify(const void* q, const void* k_cache, const void* v_
 
   auto s = reinterpret_cast<cudaStream_t>(stream);
   float* ws = static_cast<float*>(workspace);
-  cudaError_t e = tv::use_tensor_cores(dtype) ? tv::launch_attn_tc(p, plan, ws, s)
-                                              : tv::launch_attn_simt(p, plan, ws, s);
+  const bool tc = tv::use_tensor_cores(dtype);
+  cudaError_t e = tc ? tv::launch_attn_tc(p, plan, ws, s) : tv::launch_attn_simt(p, plan, ws, s);
   if (e != cudaSuccess) return TV_ERR_CUDA;
+  if (tc && plan.splits == 1) return TV_OK;  // the kernel wrote the normalised output
   return from_cuda(tv::launch_combine(p, plan, ws, s));
 }
 

@@ -26,7 +26,7 @@ int cached_sm[64];
 }  // namespace
 
 // The bf16 tensor-core kernel is switched in once it is built.
-constexpr bool kTensorCorePath = false;
+constexpr bool kTensorCorePath = true;
 
 int device_sm_count() {
   int dev = 0;
@@ -59,7 +59,9 @@ SplitPlan plan_attention(int32_t n, int32_t hq, int32_t hkv, int32_t d, int32_t 
   const int64_t kblocks = (keys + key_block - 1) / key_block;
   const int units = hkv * p.row_tiles;
   const int target = std::max(1, sm_count) * (tc ? kTcCtasPerSm : kSimtCtasPerSm);
-  int64_t s = std::max<int64_t>(1, (target + units - 1) / units);
+  // the tensor-core kernel runs one CTA per SM: stay within one wave
+  int64_t s = tc ? std::max(1, target / units)
+                 : std::max<int64_t>(1, (target + units - 1) / units);
   s = std::min<int64_t>(s, kblocks);
   const int64_t per = (kblocks + s - 1) / s;  // key blocks per split
   p.keys_per_split = (int32_t)(per * key_block);

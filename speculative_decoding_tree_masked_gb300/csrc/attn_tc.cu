@@ -1,9 +1,509 @@
-// Placeholder until the tcgen05 kernel lands: the bf16 path is not enabled.
+// Tree-masked attention on the tcgen05 tensor cores (bf16 in, fp32 accumulate).
+//
+// Split-KV flash-decoding.  A CTA owns one KV head g, up to two tiles of 128
+// query rows of g's group (row r = node * G + j is query head g * G + j of
+// tree node r / G), and one key range [kbeg, kend) of that head's prefix+tree
+// keys.  All rows of the group share every K/V block, so each block is
+// fetched once per CTA and multiplied against up to 256 rows.
+//
+// Warp roles (320 threads; every warp helps to load Q first):
+//   warp 0      TMA producer: K and V blocks of 128 keys into a 2-stage ring
+//   warp 1      TMEM allocator and MMA issuer (one thread)
+//   warps 2-5   softmax of row tile 0, warps 6-9 of tile 1; a warp reaches
+//               the TMEM lanes 32 * (warp % 4) .. + 31, which are its rows
+//
+// Tensor memory (512 columns x 128 lanes of 32 bit):
+//   S_t  columns [128 t, 128 t + 128)   scores of tile t, fp32; the softmax
+//        overwrites its first 64 columns with P (bf16 pairs), the A operand
+//        of the PV product
+//   O_t  columns [256 + D t, 256 + D t + D)   output accumulator of tile t
+//
+// Per key block j the MMA thread issues, for each tile t in turn,
+//   PV_t(j-1)  O_t += P_t . V        (A from TMEM, V from shared memory)
+//   QK_t(j)    S_t  = Q_t . K^T      (both from shared memory)
+// so that while the softmax warps of one tile work, the tensor core runs the
+// other tile's products (ping-pong).  MMAs issued by one thread complete in
+// order, so S_t(j) being complete implies PV_t(j-1) is complete: the softmax
+// may then rescale O_t in place before releasing P_t(j).
+//
+// Online softmax with a lazily moved maximum: the running maximum m used for
+// exponentiation is only raised when a block's maximum exceeds it by more
+// than 2^8 in probability, which bounds every P value by 256 and keeps the
+// result exact up to rounding while O is rarely rescaled.
+//
+// Masking: keys below the prefix length are visible to every row; tree key
+// P + t is visible to the rows of node i iff t is i or an ancestor of i (the
+// row's ancestor bitmask, built in the prologue from the parent array);
+// keys at or past kend (the split end, or P + N) are hidden.  Hidden scores
+// become -inf before the row maximum, so hidden K/V contents cannot change a
+// single output bit.  The K/V tensor maps end at row P + N, so TMA zero-fills
+// any part of a block past the tree.
+//
+// Every wait is bounded (about two seconds); on expiry the kernel records
+// TV_ERR_TIMEOUT, the other roles stop at their next wait, and the CTA frees
+// its tensor memory and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace tv {
-cudaError_t launch_attn_tc(const AttnProblem&, const SplitPlan&, float*, cudaStream_t) {
-  return cudaErrorNotSupported;
+
+namespace {
+
+constexpr int kBM = 128;         // rows per tile (TMEM lanes)
+constexpr int kBN = 128;         // keys per block
+constexpr int kTiles = 2;        // row tiles per CTA
+constexpr int kStages = 2;       // K/V ring depth
+constexpr int kThreads = 320;
+constexpr int kSoftmaxWarp0 = 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr long long kWaitCycles = 4000000000LL;
+
+struct TcParams {
+  const __nv_bfloat16* q;
+  __nv_bfloat16* out;
+  float* ws;
+  const int32_t* parent;
+  int32_t* dev_status;
+  int32_t n, hq, hkv, prefix, keys, keys_per_split, splits, rows_per_head;
+  float scale_log2;
+};
+
+template <int D>
+struct Layout {
+  static constexpr uint32_t kQTile = kBM * D * 2;   // bytes of one Q tile
+  static constexpr uint32_t kKV = kBN * D * 2;      // bytes of one K (or V) block
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kK = kQ + kTiles * kQTile;
+  static constexpr uint32_t kV = kK + kStages * kKV;
+  static constexpr uint32_t kPar = kV + kStages * kKV;
+  static constexpr uint32_t kBar = kPar + kMaxNodes * 4;
+  static constexpr uint32_t kNumBars = 3 * kTiles + 3 * kStages;
+  static constexpr uint32_t kMisc = kBar + kNumBars * 8;
+  static constexpr uint32_t kBytes = kMisc + 16;
+  static constexpr uint32_t kAlloc = kBytes + 1024;  // slack to align the base to 1024
+};
+
+struct Bars {
+  uint32_t base;
+  __device__ uint32_t s_full(int t) const { return base + 8 * t; }
+  __device__ uint32_t p_full(int t) const { return base + 8 * (kTiles + t); }
+  __device__ uint32_t o_final(int t) const { return base + 8 * (2 * kTiles + t); }
+  __device__ uint32_t k_full(int s) const { return base + 8 * (3 * kTiles + s); }
+  __device__ uint32_t v_full(int s) const { return base + 8 * (3 * kTiles + kStages + s); }
+  __device__ uint32_t kv_empty(int s) const { return base + 8 * (3 * kTiles + 2 * kStages + s); }
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         int32_t* dev_status) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      report(dev_status, TV_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
 }
+
+__device__ __forceinline__ uint32_t pick(const uint32_t (&a)[kMaskWords], int i) {
+  uint32_t w = 0u;
+#pragma unroll
+  for (int k = 0; k < kMaskWords; ++k) w = (i == k) ? a[k] : w;
+  return w;
+}
+
+// Visibility of the 32 keys [base, base + 32) to a row whose node has the
+// ancestor bitmask `anc`: bit i set iff key base + i is visible.
+__device__ __forceinline__ uint32_t visible32(const uint32_t (&anc)[kMaskWords], int prefix,
+                                              int kend, int base) {
+  const int np = prefix - base;  // prefix keys in the window
+  uint32_t vis = np >= 32 ? 0xffffffffu : (np > 0 ? (1u << np) - 1u : 0u);
+  const int lo = base - prefix;  // tree index of the window's first key
+  if (lo > -32 && lo < 32 * kMaskWords) {
+    if (lo < 0) {
+      vis |= anc[0] << (-lo);
+    } else {
+      const int wi = lo >> 5, sh = lo & 31;
+      const uint32_t a = pick(anc, wi), b = pick(anc, wi + 1);
+      vis |= sh ? __funnelshift_r(a, b, sh) : a;
+    }
+  }
+  const int ne = kend - base;  // keys before the end in the window
+  if (ne <= 0) return 0u;
+  if (ne < 32) vis &= (1u << ne) - 1u;
+  return vis;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+               const TcParams p) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base - raw);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x, g = blockIdx.z;
+  const int G = p.hq / p.hkv;
+  const int row0 = blockIdx.y * (kTiles * kBM);
+  const int ntiles = min(kTiles, (p.rows_per_head - row0 + kBM - 1) / kBM);
+  const int kbeg = split * p.keys_per_split;
+  const int kend = min(p.keys, kbeg + p.keys_per_split);
+  const int nb = (kend - kbeg + kBN - 1) / kBN;
+
+  const Bars bars{base + L::kBar};
+  int32_t* par = reinterpret_cast<int32_t*>(sm + L::kPar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 4);
+
+  if (tid == 0) {
+    for (int t = 0; t < kTiles; ++t) {
+      ptx::mbar_init(bars.s_full(t), 1);
+      ptx::mbar_init(bars.p_full(t), kBM);
+      ptx::mbar_init(bars.o_final(t), 1);
+    }
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(bars.k_full(s), 1);
+      ptx::mbar_init(bars.v_full(s), 1);
+      ptx::mbar_init(bars.kv_empty(s), 1);
+    }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::tma_prefetch_desc(&kmap);
+    ptx::tma_prefetch_desc(&vmap);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  for (int i = tid; i < p.n; i += kThreads) par[i] = p.parent[i];
+  {
+    // Q tiles into shared memory in the K-major 128-byte-swizzled layout:
+    // 64-element column chunks of [128 rows][128 B], the 16-byte piece c of
+    // row r stored at piece position c ^ (r % 8).
+    constexpr int kPieces = D / 8;
+    for (int e = tid; e < kTiles * kBM * kPieces; e += kThreads) {
+      const int t = e / (kBM * kPieces);
+      const int rem = e - t * (kBM * kPieces);
+      const int r = rem / kPieces, c = rem - r * kPieces;
+      const int grow = row0 + t * kBM + r;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (t < ntiles && grow < p.rows_per_head) {
+        const int node = grow / G, j = grow - node * G;
+        v = reinterpret_cast<const uint4*>(
+            p.q + ((size_t)node * p.hq + (size_t)g * G + j) * D)[c];
+      }
+      const uint32_t off = L::kQ + t * L::kQTile + (c >> 3) * (kBM * 128) + r * 128 +
+                           (((c & 7) ^ (r & 7)) << 4);
+      *reinterpret_cast<uint4*>(sm + off) = v;
+    }
+    ptx::fence_proxy_async_smem();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      for (int j = 0; j < nb; ++j) {
+        const int s = j % kStages, u = j / kStages;
+        if (j >= kStages && !wait_bar(bars.kv_empty(s), (u - 1) & 1, abort_flag, p.dev_status))
+          break;
+        const int key0 = kbeg + j * kBN;
+        ptx::mbar_arrive_expect_tx(bars.k_full(s), L::kKV);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          ptx::tma_load_3d(base + L::kK + s * L::kKV + c * (kBN * 128), &kmap, bars.k_full(s),
+                           c * 64, key0, g);
+        ptx::mbar_arrive_expect_tx(bars.v_full(s), L::kKV);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          ptx::tma_load_3d(base + L::kV + s * L::kKV + c * (kBN * 128), &vmap, bars.v_full(s),
+                           c * 64, key0, g);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescQK = ptx::idesc_bf16(kBM, kBN, false);
+      constexpr uint32_t kIdescPV = ptx::idesc_bf16(kBM, D, true);
+      auto issue_qk = [&](int t, int s) {
+        const uint32_t qa = base + L::kQ + t * L::kQTile;
+        const uint32_t kb = base + L::kK + s * L::kKV;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t qo = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+          const uint32_t ko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
+          ptx::mma_ss(tmem + t * kBN, ptx::smem_desc_sw128(qa + qo, 16, 1024),
+                      ptx::smem_desc_sw128(kb + ko, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int t, int s, bool acc) {
+        const uint32_t vb = base + L::kV + s * L::kKV;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          // V block, MN-major: 8-key groups 1024 B apart (SBO), the two
+          // 64-column halves of d kBN * 128 B apart (LBO)
+          ptx::mma_ts(tmem + 2 * kBN + t * D, tmem + t * kBN + kk * 8,
+                      ptx::smem_desc_sw128(vb + kk * 2048, kBN * 128, 1024), kIdescPV,
+                      (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = nb > 0 && wait_bar(bars.k_full(0), 0, abort_flag, p.dev_status);
+      if (ok) {
+        ptx::tc_fence_after();
+        for (int t = 0; t < ntiles; ++t) {
+          issue_qk(t, 0);
+          ptx::mma_commit(bars.s_full(t));
+        }
+      }
+      for (int j = 0; ok && j < nb; ++j) {
+        const int s = j % kStages, u = j / kStages;
+        for (int t = 0; t < ntiles && ok; ++t) {
+          ok = wait_bar(bars.p_full(t), j & 1, abort_flag, p.dev_status);
+          if (ok && t == 0) ok = wait_bar(bars.v_full(s), u & 1, abort_flag, p.dev_status);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_pv(t, s, j > 0);
+          if (t == ntiles - 1) ptx::mma_commit(bars.kv_empty(s));
+          if (j + 1 < nb) {
+            const int s2 = (j + 1) % kStages, u2 = (j + 1) / kStages;
+            if (t == 0) ok = wait_bar(bars.k_full(s2), u2 & 1, abort_flag, p.dev_status);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            issue_qk(t, s2);
+            ptx::mma_commit(bars.s_full(t));
+          } else {
+            ptx::mma_commit(bars.o_final(t));
+          }
+        }
+      }
+    }
+  } else if (warp >= kSoftmaxWarp0) {
+    // ------------------------------------------------------------ softmax
+    const int t = (warp - kSoftmaxWarp0) >> 2;
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int r = quarter * 32 + lane;
+    const int grow = row0 + t * kBM + r;
+    if (t < ntiles) {
+      const bool row_ok = grow < p.rows_per_head;
+      uint32_t anc[kMaskWords];
+#pragma unroll
+      for (int w = 0; w < kMaskWords; ++w) anc[w] = 0u;
+      if (row_ok && !ancestor_bits(par, grow / G, anc)) report(p.dev_status, TV_ERR_INVALID_TREE);
+      const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+      const uint32_t t_s = tmem + lane_base + t * kBN;
+      const uint32_t t_o = tmem + lane_base + 2 * kBN + t * D;
+      const float c = p.scale_log2;
+      const float rescale_raw = kRescaleLog2 / c;
+      float m_used = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < nb; ++j) {
+        ok = wait_bar(bars.s_full(t), j & 1, abort_flag, p.dev_status);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        ptx::tc_fence_after();
+        float s[kBN];
+#pragma unroll
+        for (int q = 0; q < kBN / 32; ++q) {
+          uint32_t v[32];
+          ptx::tmem_ld32(t_s + q * 32, v);
+          ptx::tmem_wait_ld(v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[q * 32 + i] = __uint_as_float(v[i]);
+        }
+        const int kb0 = kbeg + j * kBN;
+        if (kb0 + kBN > min(p.prefix, kend)) {
+#pragma unroll
+          for (int q = 0; q < kBN / 32; ++q) {
+            const uint32_t vis = visible32(anc, p.prefix, kend, kb0 + 32 * q);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (!((vis >> i) & 1u)) s[q * 32 + i] = -INFINITY;
+          }
+        }
+        float mb = s[0];
+#pragma unroll
+        for (int i = 1; i < kBN; ++i) mb = fmaxf(mb, s[i]);
+        const float m_new = fmaxf(m_used, mb);
+        const bool raise = m_new > m_used + rescale_raw;
+        float alpha = 1.f;
+        if (raise) {
+          alpha = ptx::ex2((m_used - m_new) * c);
+          m_used = m_new;
+        }
+        l *= alpha;
+        if (j > 0 && __any_sync(0xffffffffu, raise)) {
+          // O_t holds the sum through block j-1 (complete, see above)
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t v[32];
+            ptx::tmem_ld32(t_o + q * 32, v);
+            ptx::tmem_wait_ld(v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            ptx::tmem_st32(t_o + q * 32, v);
+          }
+        }
+        const float mc = (m_used == -INFINITY) ? 0.f : m_used * c;
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < kBN / 64; ++q) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float a = ptx::ex2(fmaf(s[q * 64 + 2 * i], c, -mc));
+            const float b = ptx::ex2(fmaf(s[q * 64 + 2 * i + 1], c, -mc));
+            sum += a + b;
+            pk[i] = pack_bf16x2(a, b);
+          }
+          ptx::tmem_st32(t_s + q * 32, pk);
+        }
+        l += sum;
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bars.p_full(t));
+      }
+      // epilogue: O_t is final once the last PV has completed
+      if (ok) ok = wait_bar(bars.o_final(t), 0, abort_flag, p.dev_status);
+      if (__all_sync(0xffffffffu, ok)) {
+        ptx::tc_fence_after();
+        float o[D];
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t v[32];
+          ptx::tmem_ld32(t_o + q * 32, v);
+          ptx::tmem_wait_ld(v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[q * 32 + i] = __uint_as_float(v[i]);
+        }
+        if (row_ok) {
+          const int node = grow / G, jj = grow - node * G;
+          const size_t prow = (size_t)node * p.hq + (size_t)g * G + jj;
+          if (p.splits == 1) {
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            uint4* dst = reinterpret_cast<uint4*>(p.out + prow * D);
+#pragma unroll
+            for (int q = 0; q < D / 8; ++q) {
+              uint4 w;
+              w.x = pack_bf16x2(o[8 * q + 0] * inv, o[8 * q + 1] * inv);
+              w.y = pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
+              w.z = pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
+              w.w = pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
+              dst[q] = w;
+            }
+          } else {
+            const size_t rows_all = (size_t)p.n * p.hq;
+            const size_t wrow = (size_t)split * rows_all + prow;
+            float4* dst = reinterpret_cast<float4*>(p.ws + wrow * D);
+#pragma unroll
+            for (int q = 0; q < D / 4; ++q)
+              dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            float* wm = p.ws + (size_t)p.splits * rows_all * D;
+            wm[wrow] = (m_used == -INFINITY) ? -INFINITY : m_used * c;
+            wm[(size_t)p.splits * rows_all + wrow] = l;
+          }
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// 3-D map over one layer's cache [hkv][cap][d] that ends at row `rows`
+// (= P + N): boxes of 64 columns x 128 rows x 1 head, 128-byte swizzle,
+// rows past the end read as zero.
+bool make_kv_map(CUtensorMap* map, const void* base, int d, int rows, int64_t cap, int hkv) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)hkv};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)cap * d * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kBN, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_d(const AttnProblem& p, const SplitPlan& plan, float* ws, cudaStream_t s) {
+  static bool attr_set[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Layout<D>::kAlloc);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  CUtensorMap kmap, vmap;
+  const int rows = p.prefix + p.n;
+  if (!make_kv_map(&kmap, p.k, D, rows, p.cap, p.hkv) ||
+      !make_kv_map(&vmap, p.v, D, rows, p.cap, p.hkv))
+    return cudaErrorInvalidValue;
+  TcParams tp{};
+  tp.q = static_cast<const __nv_bfloat16*>(p.q);
+  tp.out = static_cast<__nv_bfloat16*>(p.out);
+  tp.ws = ws;
+  tp.parent = p.parent;
+  tp.dev_status = p.dev_status;
+  tp.n = p.n;
+  tp.hq = p.hq;
+  tp.hkv = p.hkv;
+  tp.prefix = p.prefix;
+  tp.keys = rows;
+  tp.keys_per_split = plan.keys_per_split;
+  tp.splits = plan.splits;
+  tp.rows_per_head = (p.hq / p.hkv) * p.n;
+  tp.scale_log2 = p.scale_log2;
+  const dim3 grid(plan.splits, plan.row_tiles, p.hkv);
+  attn_tc_kernel<D><<<grid, kThreads, Layout<D>::kAlloc, s>>>(kmap, vmap, tp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_tc(const AttnProblem& p, const SplitPlan& plan, float* ws,
+                           cudaStream_t s) {
+  return p.d == 128 ? launch_d<128>(p, plan, ws, s) : launch_d<64>(p, plan, ws, s);
+}
+
 }  // namespace tv
