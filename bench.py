@@ -233,6 +233,52 @@ def run_reference(args, rank, world):
 # the GPU arm
 # --------------------------------------------------------------------------
 
+def _end_to_end(args, world, dev, stream, step, q, logits, token, parent, acc, w):
+    """Seconds for args.steps steps through the public API with the step's
+    inputs copied from pinned host memory and its result read back, plus the
+    bytes copied each way per step."""
+    import torch
+    import torch.distributed as dist
+    q_h = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    q_h.copy_(q.cpu())
+    lg_h = torch.from_numpy(w.logits).pin_memory()
+    tk_h = torch.from_numpy(w.token).pin_memory()
+    pr_h = torch.from_numpy(w.parent).pin_memory()
+    q_d, lg_d = torch.empty_like(q), torch.empty_like(logits)
+    tk_d, pr_d = torch.empty_like(token), torch.empty_like(parent)
+    res_h = {k: torch.empty(acc[k].shape, dtype=torch.int32, pin_memory=True)
+             for k in ("m", "out_tokens", "new_pos", "n_survivors")}
+    pairs = ((q_d, q_h), (lg_d, lg_h), (tk_d, tk_h), (pr_d, pr_h))
+    g_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for dst, src in pairs:
+            dst.copy_(src, non_blocking=True)
+        step(q_d, lg_d, tk_d, pr_d)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g_e2e, stream=stream):
+        step(q_d, lg_d, tk_d, pr_d)
+    h2d = sum(src.numel() * src.element_size() for _, src in pairs)
+    d2h = sum(x.numel() * x.element_size() for x in res_h.values())
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            for dst, src in pairs:
+                dst.copy_(src, non_blocking=True)
+            g_e2e.replay()
+            for k, hbuf in res_h.items():
+                hbuf.copy_(acc[k], non_blocking=True)
+            stream.synchronize()
+            _ = int(res_h["m"][0])  # the host reads the result
+    secs = time.perf_counter() - t0
+    te = torch.tensor([secs], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    return float(te.item()), h2d, d2h
+
+
 def run_gpu(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -241,15 +287,16 @@ def run_gpu(args, rank, world, local_rank):
     import speculative_decoding_tree_masked_gb300 as tvp
     from workloads import synth
 
+    layers = args.layers
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = synth.make_workload(WORKLOAD, seed=args.seed + rank, layers=LAYERS)
+    w = synth.make_workload(WORKLOAD, seed=args.seed + rank, layers=layers)
     cap = w.cap
     # inputs resident in HBM
-    kc = torch.empty((LAYERS, HKV, cap, D), dtype=torch.bfloat16, device=dev)
+    kc = torch.empty((layers, HKV, cap, D), dtype=torch.bfloat16, device=dev)
     vc = torch.empty_like(kc)
-    q = torch.empty((LAYERS, NODES, HQ, D), dtype=torch.bfloat16, device=dev)
-    for layer in range(LAYERS):
+    q = torch.empty((layers, NODES, HQ, D), dtype=torch.bfloat16, device=dev)
+    for layer in range(layers):
         ql, kl, vl = synth.make_qkv(w, layer=layer)
         q[layer].copy_(ql)
         kc[layer].copy_(kl)
@@ -257,7 +304,7 @@ def run_gpu(args, rank, world, local_rank):
     logits = torch.from_numpy(w.logits).to(dev)
     token = torch.from_numpy(w.token).to(dev)
     parent = torch.from_numpy(w.parent).to(dev)
-    out = torch.empty((LAYERS, NODES, HQ, D), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((layers, NODES, HQ, D), dtype=torch.bfloat16, device=dev)
     ws = tvp.attn_workspace(NODES, HQ, HKV, D, torch.bfloat16, PREFIX, dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     acc = {k: torch.empty(sz, dtype=torch.int32, device=dev) for k, sz in (
@@ -266,14 +313,14 @@ def run_gpu(args, rank, world, local_rank):
     stream = torch.cuda.Stream(dev)
 
     def step(qs=q, lg=logits, tk=token, pr=parent):
-        for layer in range(LAYERS):
+        for layer in range(layers):
             tvp.tree_attn_verify(qs[layer], kc[layer], vc[layer], PREFIX, pr, out=out[layer],
                                  workspace=ws, status=status)
         tvp.tree_accept(lg, tk, pr, PREFIX, outs=acc, status=status)
         tvp.kv_compact(kc, vc, PREFIX, NODES, acc["new_pos"], status=status)
 
     def attention_only():
-        for layer in range(LAYERS):
+        for layer in range(layers):
             tvp.tree_attn_verify(q[layer], kc[layer], vc[layer], PREFIX, parent, out=out[layer],
                                  workspace=ws, status=status)
 
@@ -288,7 +335,9 @@ def run_gpu(args, rank, world, local_rank):
     with torch.cuda.graph(g_attn, stream=stream):
         attention_only()
     torch.cuda.synchronize()
-    launches_per_step = LAYERS * 2 + 2 + 1  # attention + combine per layer, argmax, walk, compact
+    splits = _attn_splits(tvp)
+    per_layer_launches = 1 if splits == 1 else 2  # attention (+ combine)
+    launches_per_step = layers * per_layer_launches + 2 + 1  # argmax, walk, compact
 
     def barrier():
         if world > 1:
@@ -315,7 +364,7 @@ def run_gpu(args, rank, world, local_rank):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
     total_ms = float(t.item())
 
-    # the dominant kernel alone: 80 layers of attention, events on its stream
+    # the dominant kernel alone: every layer's attention call, events on its stream
     reps = max(3, args.steps)
     with torch.cuda.stream(stream):
         g_attn.replay()
@@ -325,47 +374,11 @@ def run_gpu(args, rank, world, local_rank):
             g_attn.replay()
         eb.record(stream)
     torch.cuda.synchronize()
-    attn_ms_layer = ea.elapsed_time(eb) / (reps * LAYERS)
+    attn_ms_layer = ea.elapsed_time(eb) / (reps * layers)
 
-    # end to end through the public API: step inputs from pinned host memory,
-    # the step's result read back
-    q_h = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
-    q_h.copy_(q.cpu())
-    lg_h = torch.from_numpy(w.logits).pin_memory()
-    tk_h = torch.from_numpy(w.token).pin_memory()
-    pr_h = torch.from_numpy(w.parent).pin_memory()
-    q_d, lg_d, tk_d, pr_d = torch.empty_like(q), torch.empty_like(logits), torch.empty_like(
-        token), torch.empty_like(parent)
-    res_h = {k: torch.empty(acc[k].shape, dtype=torch.int32, pin_memory=True)
-             for k in ("m", "out_tokens", "new_pos", "n_survivors")}
-    g_e2e = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        for dst, src in ((q_d, q_h), (lg_d, lg_h), (tk_d, tk_h), (pr_d, pr_h)):
-            dst.copy_(src, non_blocking=True)
-        step(q_d, lg_d, tk_d, pr_d)
-    torch.cuda.synchronize()
-    with torch.cuda.graph(g_e2e, stream=stream):
-        step(q_d, lg_d, tk_d, pr_d)
-    h2d = sum(x.numel() * x.element_size() for x in (q_h, lg_h, tk_h, pr_h))
-    d2h = sum(x.numel() * x.element_size() for x in res_h.values())
-    barrier()
-    t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for _ in range(args.steps):
-            q_d.copy_(q_h, non_blocking=True)
-            lg_d.copy_(lg_h, non_blocking=True)
-            tk_d.copy_(tk_h, non_blocking=True)
-            pr_d.copy_(pr_h, non_blocking=True)
-            g_e2e.replay()
-            for k, hbuf in res_h.items():
-                hbuf.copy_(acc[k], non_blocking=True)
-            stream.synchronize()
-            _ = int(res_h["m"][0])  # the host reads the result
-    e2e_s = time.perf_counter() - t0
-    te = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_s = float(te.item())
+    e2e = None
+    if not args.no_e2e:
+        e2e = _end_to_end(args, world, dev, stream, step, q, logits, token, parent, acc, w)
 
     torch.cuda.synchronize()
     if int(status.item()) != 0:
@@ -379,7 +392,7 @@ def run_gpu(args, rank, world, local_rank):
     t_layer = attn_ms_layer * 1e-3
     gbs = nbytes / t_layer / 1e9
     tflops = flops / t_layer / 1e12
-    tensor_path = tvp.lib().tv_attn_uses_tensor_cores(tvp.TV_BF16) != 0
+    tensor_path = tvp.lib().tv_attn_uses_tensor_cores(tvp.TV_BF16) == 1
     if tensor_path:
         roof = {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s"}
@@ -390,8 +403,9 @@ def run_gpu(args, rank, world, local_rank):
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = _profiled_traffic()
     roof["peak_source"] = peaks["source"] + " (burst)"
-    roof["kernel"] = "tree attention per layer (split-KV partials + combine)"
-    roof["per_launch"] = {"bytes": nbytes, "flops": flops, "us": attn_ms_layer * 1e3}
+    roof["kernel"] = "tree attention, one layer (split-KV tcgen05 kernel + combine)"
+    roof["per_launch"] = {"bytes": nbytes, "flops": flops, "us": attn_ms_layer * 1e3,
+                          "splits": splits}
 
     if args.no_cpu_baseline:
         cpu = None
@@ -402,13 +416,17 @@ def run_gpu(args, rank, world, local_rank):
 
     ms = total_ms / args.steps
     line = _line_base(args, world)
+    if layers != LAYERS:
+        line["config"]["layers"] = layers
+        line["config"]["workload"] += f" (profiling case: {layers} layers)"
     line.update({
         "value": world * NODES * args.steps / (total_ms * 1e-3),
         "ms_per_step": ms,
         "roofline": roof,
         "cpu_baseline": cpu,
-        "e2e": {"value": world * NODES * args.steps / e2e_s, "unit": "tree tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": None if e2e is None else {
+            "value": world * NODES * args.steps / e2e[0], "unit": "tree tokens/s",
+            "h2d_bytes_per_step": e2e[1], "d2h_bytes_per_step": e2e[2]},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(peaks["sm_max_mhz"]),
         "verify_steps_per_s": world * 1e3 / ms,
@@ -421,6 +439,14 @@ def run_gpu(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def _attn_splits(tvp):
+    """Split count the library plans for this workload (from the workspace
+    size: splits * rows * (d + 2) * 4 bytes, rounded up to 256)."""
+    rows = NODES * HQ
+    nbytes = tvp.attn_workspace_size(NODES, HQ, HKV, D, __import__("torch").bfloat16, PREFIX)
+    return max(1, nbytes // (rows * (D + 2) * 4))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -429,6 +455,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=LAYERS,
+                    help="layers of KV per step (a smaller case for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -82,11 +82,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   const float* mrow = ws + (size_t)splits * rows * D;
   const float* lrow = mrow + (size_t)splits * rows;
   float M = -INFINITY;
+#pragma unroll 4
   for (int s = 0; s < splits; ++s) M = fmaxf(M, mrow[(size_t)s * rows + row]);
   float L = 0.f;
   float o[C];
 #pragma unroll
   for (int c = 0; c < C; ++c) o[c] = 0.f;
+#pragma unroll 4
   for (int s = 0; s < splits; ++s) {
     const float ms = mrow[(size_t)s * rows + row];
     const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);

@@ -186,8 +186,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     }
     *abort_flag = 0;
     ptx::fence_mbar_init();
-    ptx::tma_prefetch_desc(&kmap);
-    ptx::tma_prefetch_desc(&vmap);
+  }
+  // The producer thread (tid 0) starts streaming K/V at once: the first
+  // kStages blocks need no free slot and do not depend on Q.
+  auto load_block = [&](int j) {
+    const int s = j % kStages;
+    const int key0 = kbeg + j * kBN;
+    ptx::mbar_arrive_expect_tx(bars.k_full(s), L::kKV);
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c)
+      ptx::tma_load_3d(base + L::kK + s * L::kKV + c * (kBN * 128), &kmap, bars.k_full(s), c * 64,
+                       key0, g);
+    ptx::mbar_arrive_expect_tx(bars.v_full(s), L::kKV);
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c)
+      ptx::tma_load_3d(base + L::kV + s * L::kKV + c * (kBN * 128), &vmap, bars.v_full(s), c * 64,
+                       key0, g);
+  };
+  if (tid == 0) {
+    for (int j = 0; j < min(nb, kStages); ++j) load_block(j);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
@@ -197,22 +214,39 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   {
     // Q tiles into shared memory in the K-major 128-byte-swizzled layout:
     // 64-element column chunks of [128 rows][128 B], the 16-byte piece c of
-    // row r stored at piece position c ^ (r % 8).
+    // row r stored at piece position c ^ (r % 8).  All loads of a thread are
+    // issued before its stores so that their latencies overlap.
     constexpr int kPieces = D / 8;
-    for (int e = tid; e < kTiles * kBM * kPieces; e += kThreads) {
-      const int t = e / (kBM * kPieces);
-      const int rem = e - t * (kBM * kPieces);
-      const int r = rem / kPieces, c = rem - r * kPieces;
-      const int grow = row0 + t * kBM + r;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (t < ntiles && grow < p.rows_per_head) {
-        const int node = grow / G, j = grow - node * G;
-        v = reinterpret_cast<const uint4*>(
-            p.q + ((size_t)node * p.hq + (size_t)g * G + j) * D)[c];
+    constexpr int kTotal = kTiles * kBM * kPieces;
+    constexpr int kPer = (kTotal + kThreads - 1) / kThreads;
+    uint4 v[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = tid + i * kThreads;
+      v[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (e < kTotal) {
+        const int t = e / (kBM * kPieces);
+        const int rem = e - t * (kBM * kPieces);
+        const int r = rem / kPieces, c = rem - r * kPieces;
+        const int grow = row0 + t * kBM + r;
+        if (t < ntiles && grow < p.rows_per_head) {
+          const int node = grow / G, j = grow - node * G;
+          v[i] = __ldg(reinterpret_cast<const uint4*>(
+                           p.q + ((size_t)node * p.hq + (size_t)g * G + j) * D) + c);
+        }
       }
-      const uint32_t off = L::kQ + t * L::kQTile + (c >> 3) * (kBM * 128) + r * 128 +
-                           (((c & 7) ^ (r & 7)) << 4);
-      *reinterpret_cast<uint4*>(sm + off) = v;
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = tid + i * kThreads;
+      if (e < kTotal) {
+        const int t = e / (kBM * kPieces);
+        const int rem = e - t * (kBM * kPieces);
+        const int r = rem / kPieces, c = rem - r * kPieces;
+        const uint32_t off = L::kQ + t * L::kQTile + (c >> 3) * (kBM * 128) + r * 128 +
+                             (((c & 7) ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(sm + off) = v[i];
+      }
     }
     ptx::fence_proxy_async_smem();
   }
@@ -224,21 +258,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      for (int j = 0; j < nb; ++j) {
+      for (int j = kStages; j < nb; ++j) {
         const int s = j % kStages, u = j / kStages;
-        if (j >= kStages && !wait_bar(bars.kv_empty(s), (u - 1) & 1, abort_flag, p.dev_status))
-          break;
-        const int key0 = kbeg + j * kBN;
-        ptx::mbar_arrive_expect_tx(bars.k_full(s), L::kKV);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          ptx::tma_load_3d(base + L::kK + s * L::kKV + c * (kBN * 128), &kmap, bars.k_full(s),
-                           c * 64, key0, g);
-        ptx::mbar_arrive_expect_tx(bars.v_full(s), L::kKV);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          ptx::tma_load_3d(base + L::kV + s * L::kKV + c * (kBN * 128), &vmap, bars.v_full(s),
-                           c * 64, key0, g);
+        if (!wait_bar(bars.kv_empty(s), (u - 1) & 1, abort_flag, p.dev_status)) break;
+        load_block(j);
       }
     }
   } else if (warp == 1) {
@@ -321,15 +344,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         ok = wait_bar(bars.s_full(t), j & 1, abort_flag, p.dev_status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         ptx::tc_fence_after();
-        float s[kBN];
-#pragma unroll
-        for (int q = 0; q < kBN / 32; ++q) {
-          uint32_t v[32];
-          ptx::tmem_ld32(t_s + q * 32, v);
-          ptx::tmem_wait_ld(v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[q * 32 + i] = __uint_as_float(v[i]);
-        }
+        uint32_t sv[kBN];
+        ptx::tmem_ld128(t_s, sv);
+        ptx::tmem_wait_ld(sv);
+        float* s = reinterpret_cast<float*>(sv);
         const int kb0 = kbeg + j * kBN;
         if (kb0 + kBN > min(p.prefix, kend)) {
 #pragma unroll
@@ -340,9 +358,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
               if (!((vis >> i) & 1u)) s[q * 32 + i] = -INFINITY;
           }
         }
-        float mb = s[0];
+        float mx[8];
 #pragma unroll
-        for (int i = 1; i < kBN; ++i) mb = fmaxf(mb, s[i]);
+        for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+        for (int i = 8; i < kBN; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+        const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         const float m_new = fmaxf(m_used, mb);
         const bool raise = m_new > m_used + rescale_raw;
         float alpha = 1.f;
@@ -350,9 +372,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           alpha = ptx::ex2((m_used - m_new) * c);
           m_used = m_new;
         }
-        l *= alpha;
+        const float mc = (m_used == -INFINITY) ? 0.f : m_used * c;
+        float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+        for (int q = 0; q < kBN / 32; ++q) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float a = ptx::ex2(fmaf(s[q * 32 + 2 * i], c, -mc));
+            const float b = ptx::ex2(fmaf(s[q * 32 + 2 * i + 1], c, -mc));
+            sum0 += a;
+            sum1 += b;
+            pk[i] = pack_bf16x2(a, b);
+          }
+          ptx::tmem_st16(t_s + q * 16, pk);
+        }
+        l = l * alpha + (sum0 + sum1);
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
-          // O_t holds the sum through block j-1 (complete, see above)
+          // O_t holds the sum through block j-1 (complete, see above) and
+          // PV_t(j) waits for this thread's P_full arrival
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
             uint32_t v[32];
@@ -363,21 +401,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             ptx::tmem_st32(t_o + q * 32, v);
           }
         }
-        const float mc = (m_used == -INFINITY) ? 0.f : m_used * c;
-        float sum = 0.f;
-#pragma unroll
-        for (int q = 0; q < kBN / 64; ++q) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float a = ptx::ex2(fmaf(s[q * 64 + 2 * i], c, -mc));
-            const float b = ptx::ex2(fmaf(s[q * 64 + 2 * i + 1], c, -mc));
-            sum += a + b;
-            pk[i] = pack_bf16x2(a, b);
-          }
-          ptx::tmem_st32(t_s + q * 32, pk);
-        }
-        l += sum;
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bars.p_full(t));
