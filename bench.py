@@ -440,11 +440,12 @@ def run_gpu(args, rank, world, local_rank):
 
 
 def _attn_splits(tvp):
-    """Split count the library plans for this workload (from the workspace
-    size: splits * rows * (d + 2) * 4 bytes, rounded up to 256)."""
+    """Split count the library plans for this workload, read off the
+    workspace size: per split, a 4-byte log-sum-exp and a d-wide fp16
+    partial for each of the n * hq rows (plus padding below 512 bytes)."""
     rows = NODES * HQ
     nbytes = tvp.attn_workspace_size(NODES, HQ, HKV, D, __import__("torch").bfloat16, PREFIX)
-    return max(1, nbytes // (rows * (D + 2) * 4))
+    return max(1, nbytes // (rows * (2 * D + 4)))
 
 
 def main():

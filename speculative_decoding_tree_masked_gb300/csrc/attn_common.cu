@@ -1,13 +1,15 @@
 // Split-KV planning and the combine step of tree-masked attention.
 //
 // Flash-decoding: the key range [0, P + N) of every (KV head, row tile) is cut
-// into `splits` chunks processed by different CTAs; each writes an unnormalised
-// partial output with its row maximum and row sum, and the combine kernel
-// merges them with log-sum-exp weights:
-//   O = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s,   M = max_s m_s.
-// (m in log2 units: scores are pre-multiplied by scale * log2(e).)
+// into `splits` chunks processed by different CTAs; each writes its
+// normalised partial output O_s and the log2 of its softmax denominator
+// lse_s, and the combine kernel merges them with log-sum-exp weights:
+//   O = sum_s 2^(lse_s - M) O_s / sum_s 2^(lse_s - M),   M = max_s lse_s.
+// (log2 units: scores are pre-multiplied by scale * log2(e).)
 #include <algorithm>
 #include <cmath>
+
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -67,42 +69,59 @@ SplitPlan plan_attention(int32_t n, int32_t hq, int32_t hkv, int32_t d, int32_t 
   p.keys_per_split = (int32_t)(per * key_block);
   p.splits = (int32_t)((kblocks + per - 1) / per);
   const size_t rows_all = (size_t)n * hq;
-  p.ws_bytes = ((size_t)p.splits * rows_all * (size_t)(d + 2) * sizeof(float) + 255) & ~size_t(255);
+  const size_t o_elem = tc ? 2 : 4;  // fp16 partials for bf16, fp32 for fp32
+  p.ws_bytes = (partial_o_offset(p.splits, rows_all) + (size_t)p.splits * rows_all * d * o_elem +
+                255) & ~size_t(255);
   return p;
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ ws, int splits,
+__device__ __forceinline__ void load_partial(const float* p, float (&o)[4]) {
+  const float4 x = *reinterpret_cast<const float4*>(p);
+  o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
+}
+__device__ __forceinline__ void load_partial(const float* p, float (&o)[2]) {
+  const float2 x = *reinterpret_cast<const float2*>(p);
+  o[0] = x.x; o[1] = x.y;
+}
+__device__ __forceinline__ void load_partial(const __half* p, float (&o)[4]) {
+  const uint2 x = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&x.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&x.y));
+  o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+}
+__device__ __forceinline__ void load_partial(const __half* p, float (&o)[2]) {
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(p));
+  o[0] = a.x; o[1] = a.y;
+}
+
+// One warp per output row: O = sum_s 2^(lse_s - M) O_s / sum_s 2^(lse_s - M).
+template <typename PT, typename T, int D>
+__global__ void __launch_bounds__(256) combine_kernel(const uint8_t* __restrict__ ws, int splits,
                                                       int rows, T* __restrict__ out) {
   constexpr int C = D / 32;  // consecutive columns per lane
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
-  const float* acc = ws;
-  const float* mrow = ws + (size_t)splits * rows * D;
-  const float* lrow = mrow + (size_t)splits * rows;
+  const float* lse = reinterpret_cast<const float*>(ws);
+  const PT* po = reinterpret_cast<const PT*>(ws + partial_o_offset(splits, rows));
   float M = -INFINITY;
 #pragma unroll 4
-  for (int s = 0; s < splits; ++s) M = fmaxf(M, mrow[(size_t)s * rows + row]);
-  float L = 0.f;
+  for (int s = 0; s < splits; ++s) M = fmaxf(M, lse[(size_t)s * rows + row]);
+  float W = 0.f;
   float o[C];
 #pragma unroll
   for (int c = 0; c < C; ++c) o[c] = 0.f;
 #pragma unroll 4
   for (int s = 0; s < splits; ++s) {
-    const float ms = mrow[(size_t)s * rows + row];
-    const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-    L += w * lrow[(size_t)s * rows + row];
-    const float* a = acc + ((size_t)s * rows + row) * D + lane * C;
-    if constexpr (C == 4) {
-      const float4 x = *reinterpret_cast<const float4*>(a);
-      o[0] += w * x.x; o[1] += w * x.y; o[2] += w * x.z; o[3] += w * x.w;
-    } else {
+    const float ls = lse[(size_t)s * rows + row];
+    const float w = (ls == -INFINITY) ? 0.f : exp2f(ls - M);
+    W += w;
+    float x[C];
+    load_partial(po + ((size_t)s * rows + row) * D + lane * C, x);
 #pragma unroll
-      for (int c = 0; c < C; ++c) o[c] += w * a[c];
-    }
+    for (int c = 0; c < C; ++c) o[c] = fmaf(w, x[c], o[c]);
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const float inv = W > 0.f ? 1.f / W : 0.f;
   T* dst = out + (size_t)row * D + lane * C;
 #pragma unroll
   for (int c = 0; c < C; ++c) store_f32(dst + c, o[c] * inv);
@@ -112,14 +131,15 @@ cudaError_t launch_combine(const AttnProblem& p, const SplitPlan& plan, const fl
                            cudaStream_t s) {
   const int rows = p.n * p.hq;
   const dim3 grid((rows + 7) / 8), block(256);
+  const auto* w = reinterpret_cast<const uint8_t*>(ws);
   if (p.dtype == TV_BF16) {
     auto* out = static_cast<__nv_bfloat16*>(p.out);
-    if (p.d == 128) combine_kernel<__nv_bfloat16, 128><<<grid, block, 0, s>>>(ws, plan.splits, rows, out);
-    else combine_kernel<__nv_bfloat16, 64><<<grid, block, 0, s>>>(ws, plan.splits, rows, out);
+    if (p.d == 128) combine_kernel<__half, __nv_bfloat16, 128><<<grid, block, 0, s>>>(w, plan.splits, rows, out);
+    else combine_kernel<__half, __nv_bfloat16, 64><<<grid, block, 0, s>>>(w, plan.splits, rows, out);
   } else {
     auto* out = static_cast<float*>(p.out);
-    if (p.d == 128) combine_kernel<float, 128><<<grid, block, 0, s>>>(ws, plan.splits, rows, out);
-    else combine_kernel<float, 64><<<grid, block, 0, s>>>(ws, plan.splits, rows, out);
+    if (p.d == 128) combine_kernel<float, float, 128><<<grid, block, 0, s>>>(w, plan.splits, rows, out);
+    else combine_kernel<float, float, 64><<<grid, block, 0, s>>>(w, plan.splits, rows, out);
   }
   return cudaGetLastError();
 }

@@ -135,21 +135,19 @@ attn_simt_kernel(const AttnProblem p, const int keys_per_split, float* __restric
   }
 
   const int rows_all = p.n * p.hq;
-  float* wacc = ws;
-  float* wm = ws + (size_t)splits * rows_all * D;
-  float* wl = wm + (size_t)splits * rows_all;
+  float* wlse = ws;
+  float* wo = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) +
+                                       partial_o_offset(splits, rows_all));
 #pragma unroll
   for (int rr = 0; rr < kRowsPerWarp; ++rr) {
     const int r = r0 + warp * kRowsPerWarp + rr;
     if (r >= rows_total) continue;
     const int node = r / G, j = r % G;
     const size_t prow = (size_t)split * rows_all + (size_t)node * p.hq + (size_t)g * G + j;
+    const float inv = l[rr] > 0.f ? 1.f / l[rr] : 0.f;
 #pragma unroll
-    for (int c = 0; c < C; ++c) wacc[prow * D + lane + 32 * c] = acc[rr][c];
-    if (lane == 0) {
-      wm[prow] = m[rr];
-      wl[prow] = l[rr];
-    }
+    for (int c = 0; c < C; ++c) wo[prow * D + lane + 32 * c] = acc[rr][c] * inv;
+    if (lane == 0) wlse[prow] = l[rr] > 0.f ? m[rr] + log2f(l[rr]) : -INFINITY;
   }
 }
 

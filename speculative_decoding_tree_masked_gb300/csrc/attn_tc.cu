@@ -6,11 +6,12 @@
 // keys.  All rows of the group share every K/V block, so each block is
 // fetched once per CTA and multiplied against up to 256 rows.
 //
-// Warp roles (320 threads; every warp helps to load Q first):
+// Warp roles (576 threads; every warp helps to load Q first):
 //   warp 0      TMA producer: K and V blocks of 128 keys into a 2-stage ring
 //   warp 1      TMEM allocator and MMA issuer (one thread)
-//   warps 2-5   softmax of row tile 0, warps 6-9 of tile 1; a warp reaches
-//               the TMEM lanes 32 * (warp % 4) .. + 31, which are its rows
+//   warps 2-9   softmax of row tile 0, warps 10-17 of tile 1: two warps per
+//               32-row quarter, each on half of the key columns; a warp
+//               reaches the TMEM lanes 32 * (warp % 4) .. + 31, its rows
 //
 // Tensor memory (512 columns x 128 lanes of 32 bit):
 //   S_t  columns [128 t, 128 t + 128)   scores of tile t, fp32; the softmax
@@ -45,6 +46,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cuda_fp16.h>
+
 #include <cmath>
 
 #include "common.cuh"
@@ -57,9 +60,10 @@ namespace {
 
 constexpr int kBM = 128;         // rows per tile (TMEM lanes)
 constexpr int kBN = 128;         // keys per block
+constexpr int kHalf = kBN / 2;   // key columns per softmax warp
 constexpr int kTiles = 2;        // row tiles per CTA
 constexpr int kStages = 2;       // K/V ring depth
-constexpr int kThreads = 320;
+constexpr int kThreads = 576;
 constexpr int kSoftmaxWarp0 = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
@@ -68,7 +72,7 @@ constexpr long long kWaitCycles = 4000000000LL;
 struct TcParams {
   const __nv_bfloat16* q;
   __nv_bfloat16* out;
-  float* ws;
+  float* ws;  // lse [splits][rows], then fp16 partials (see internal.h)
   const int32_t* parent;
   int32_t* dev_status;
   int32_t n, hq, hkv, prefix, keys, keys_per_split, splits, rows_per_head;
@@ -83,8 +87,9 @@ struct Layout {
   static constexpr uint32_t kK = kQ + kTiles * kQTile;
   static constexpr uint32_t kV = kK + kStages * kKV;
   static constexpr uint32_t kPar = kV + kStages * kKV;
-  static constexpr uint32_t kBar = kPar + kMaxNodes * 4;
-  static constexpr uint32_t kNumBars = 3 * kTiles + 3 * kStages;
+  static constexpr uint32_t kXch = kPar + kMaxNodes * 4;   // [tile][half][row] floats
+  static constexpr uint32_t kBar = kXch + kTiles * 2 * kBM * 4;
+  static constexpr uint32_t kNumBars = 3 * kTiles + 3 * kStages + kTiles * 4 + kTiles;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kMisc + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // slack to align the base to 1024
@@ -98,6 +103,12 @@ struct Bars {
   __device__ uint32_t k_full(int s) const { return base + 8 * (3 * kTiles + s); }
   __device__ uint32_t v_full(int s) const { return base + 8 * (3 * kTiles + kStages + s); }
   __device__ uint32_t kv_empty(int s) const { return base + 8 * (3 * kTiles + 2 * kStages + s); }
+  // exchange between the two softmax warps of one (tile, row quarter)
+  __device__ uint32_t xchg(int t, int q) const {
+    return base + 8 * (3 * kTiles + 3 * kStages + 4 * t + q);
+  }
+  // every softmax thread of tile t has staged its output row
+  __device__ uint32_t epi(int t) const { return base + 8 * (7 * kTiles + 3 * kStages + t); }
 };
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -149,6 +160,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -176,13 +192,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   if (tid == 0) {
     for (int t = 0; t < kTiles; ++t) {
       ptx::mbar_init(bars.s_full(t), 1);
-      ptx::mbar_init(bars.p_full(t), kBM);
+      ptx::mbar_init(bars.p_full(t), 2 * kBM);
       ptx::mbar_init(bars.o_final(t), 1);
     }
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(bars.k_full(s), 1);
       ptx::mbar_init(bars.v_full(s), 1);
       ptx::mbar_init(bars.kv_empty(s), 1);
+    }
+    for (int t = 0; t < kTiles; ++t) {
+      for (int q = 0; q < 4; ++q) ptx::mbar_init(bars.xchg(t, q), 64);
+      ptx::mbar_init(bars.epi(t), 2 * kBM);
     }
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -203,9 +223,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       ptx::tma_load_3d(base + L::kV + s * L::kKV + c * (kBN * 128), &vmap, bars.v_full(s), c * 64,
                        key0, g);
   };
-  if (tid == 0) {
-    for (int j = 0; j < min(nb, kStages); ++j) load_block(j);
-  }
+  if (tid == 0 && nb > 0) load_block(0);
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
     ptx::tmem_relinquish();
@@ -258,9 +276,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      for (int j = kStages; j < nb; ++j) {
+      // block 1 is requested once block 0's keys have landed, so that the
+      // first block of every CTA reaches the SMs ahead of the rest
+      for (int j = 1; j < nb; ++j) {
         const int s = j % kStages, u = j / kStages;
-        if (!wait_bar(bars.kv_empty(s), (u - 1) & 1, abort_flag, p.dev_status)) break;
+        const bool ready = j < kStages
+                               ? wait_bar(bars.k_full(0), 0, abort_flag, p.dev_status)
+                               : wait_bar(bars.kv_empty(s), (u - 1) & 1, abort_flag, p.dev_status);
+        if (!ready) break;
         load_block(j);
       }
     }
@@ -323,10 +346,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     }
   } else if (warp >= kSoftmaxWarp0) {
     // ------------------------------------------------------------ softmax
-    const int t = (warp - kSoftmaxWarp0) >> 2;
+    // Two warps share each 32-row quarter of a tile: half h takes the key
+    // columns [64 h, 64 h + 64) of S and the output columns [D/2 h, D/2 (h+1))
+    // of O.  They trade partial row maxima (and finally row sums) through
+    // shared memory, synchronised by a 64-arrival mbarrier (bounded waits).
+    const int sw = warp - kSoftmaxWarp0;
+    const int t = sw >> 3;
+    const int h = (sw >> 2) & 1;
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;
     const int grow = row0 + t * kBM + r;
+    const uint32_t pair_bar = bars.xchg(t, quarter);
+    float* xch = reinterpret_cast<float*>(sm + L::kXch) + (t * 2 + h) * kBM;
+    const float* xch_other = reinterpret_cast<const float*>(sm + L::kXch) + (t * 2 + (1 - h)) * kBM;
     if (t < ntiles) {
       const bool row_ok = grow < p.rows_per_head;
       uint32_t anc[kMaskWords];
@@ -335,7 +367,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       if (row_ok && !ancestor_bits(par, grow / G, anc)) report(p.dev_status, TV_ERR_INVALID_TREE);
       const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
       const uint32_t t_s = tmem + lane_base + t * kBN;
-      const uint32_t t_o = tmem + lane_base + 2 * kBN + t * D;
+      const uint32_t t_o = tmem + lane_base + 2 * kBN + t * D + h * (D / 2);
       const float c = p.scale_log2;
       const float rescale_raw = kRescaleLog2 / c;
       float m_used = -INFINITY, l = 0.f;
@@ -344,14 +376,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         ok = wait_bar(bars.s_full(t), j & 1, abort_flag, p.dev_status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         ptx::tc_fence_after();
-        uint32_t sv[kBN];
-        ptx::tmem_ld128(t_s, sv);
+        uint32_t sv[kHalf];
+        ptx::tmem_ld64(t_s + h * kHalf, sv);
         ptx::tmem_wait_ld(sv);
         float* s = reinterpret_cast<float*>(sv);
-        const int kb0 = kbeg + j * kBN;
-        if (kb0 + kBN > min(p.prefix, kend)) {
+        const int kb0 = kbeg + j * kBN + h * kHalf;
+        if (kb0 + kHalf > min(p.prefix, kend)) {
 #pragma unroll
-          for (int q = 0; q < kBN / 32; ++q) {
+          for (int q = 0; q < kHalf / 32; ++q) {
             const uint32_t vis = visible32(anc, p.prefix, kend, kb0 + 32 * q);
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -362,9 +394,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = s[i];
 #pragma unroll
-        for (int i = 8; i < kBN; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
-        const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+        for (int i = 8; i < kHalf; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+        const float pm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        // both halves must have read S before either overwrites it with P,
+        // and need each other's maximum: one barrier does both
+        xch[r] = pm;
+        ptx::mbar_arrive(pair_bar);
+        ok = wait_bar(pair_bar, j & 1, abort_flag, p.dev_status);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        const float mb = fmaxf(pm, xch_other[r]);
         const float m_new = fmaxf(m_used, mb);
         const bool raise = m_new > m_used + rescale_raw;
         float alpha = 1.f;
@@ -375,7 +414,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         const float mc = (m_used == -INFINITY) ? 0.f : m_used * c;
         float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
-        for (int q = 0; q < kBN / 32; ++q) {
+        for (int q = 0; q < kHalf / 32; ++q) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -385,14 +424,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             sum1 += b;
             pk[i] = pack_bf16x2(a, b);
           }
-          ptx::tmem_st16(t_s + q * 16, pk);
+          ptx::tmem_st16(t_s + h * (kHalf / 2) + q * 16, pk);
         }
         l = l * alpha + (sum0 + sum1);
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
           // O_t holds the sum through block j-1 (complete, see above) and
           // PV_t(j) waits for this thread's P_full arrival
 #pragma unroll
-          for (int q = 0; q < D / 32; ++q) {
+          for (int q = 0; q < D / 64; ++q) {
             uint32_t v[32];
             ptx::tmem_ld32(t_o + q * 32, v);
             ptx::tmem_wait_ld(v);
@@ -404,45 +443,82 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bars.p_full(t));
+        // the next block's exchange slot is written only after the partner
+        // has read this one: the partner's read precedes its P_full arrival,
+        // and this thread's next write follows the next S_full wait, which
+        // needs every arrival
       }
       // epilogue: O_t is final once the last PV has completed
       if (ok) ok = wait_bar(bars.o_final(t), 0, abort_flag, p.dev_status);
+      // row sum = the two halves' sums (same m_used in both); the partner
+      // read this slot's last maximum before its final P_full arrival, which
+      // the final PV (and so o_final) waited for
+      if (ok) {
+        xch[r] = l;
+        ptx::mbar_arrive(pair_bar);
+        ok = wait_bar(pair_bar, nb & 1, abort_flag, p.dev_status);
+        l += xch_other[r];
+      }
+      // Stage this thread's normalised half-row as 16-bit values in shared
+      // memory (the Q tiles are free: every MMA has completed), then copy the
+      // tile out with coalesced 16-byte stores.  Row R's 16-byte chunk k sits
+      // at chunk position (k + R) % kChunks, which spreads a warp's stores
+      // over all banks.  With one split the result is the final bf16 output;
+      // otherwise it is the split's fp16 partial plus its log-sum-exp.
+      constexpr int kChunks = D / 8;
+      const bool to_out = p.splits == 1;
+      const size_t rows_all = (size_t)p.n * p.hq;
+      const int R = t * kBM + r;
       if (__all_sync(0xffffffffu, ok)) {
         ptx::tc_fence_after();
-        float o[D];
+        float o[D / 2];
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
+        for (int q = 0; q < D / 64; ++q) {
           uint32_t v[32];
           ptx::tmem_ld32(t_o + q * 32, v);
           ptx::tmem_wait_ld(v);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[q * 32 + i] = __uint_as_float(v[i]);
         }
-        if (row_ok) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint8_t* srow = sm + L::kQ + (size_t)R * (D * 2);
+#pragma unroll
+        for (int q = 0; q < kChunks / 2; ++q) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float a = o[8 * q + 2 * e] * inv, b = o[8 * q + 2 * e + 1] * inv;
+            w[e] = to_out ? pack_bf16x2(a, b) : pack_f16x2(a, b);
+          }
+          const int k = h * (kChunks / 2) + q;
+          *reinterpret_cast<uint4*>(srow + ((k + R) % kChunks) * 16) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        if (!to_out && h == 0 && row_ok) {
           const int node = grow / G, jj = grow - node * G;
           const size_t prow = (size_t)node * p.hq + (size_t)g * G + jj;
-          if (p.splits == 1) {
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            uint4* dst = reinterpret_cast<uint4*>(p.out + prow * D);
-#pragma unroll
-            for (int q = 0; q < D / 8; ++q) {
-              uint4 w;
-              w.x = pack_bf16x2(o[8 * q + 0] * inv, o[8 * q + 1] * inv);
-              w.y = pack_bf16x2(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
-              w.z = pack_bf16x2(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
-              w.w = pack_bf16x2(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
-              dst[q] = w;
-            }
-          } else {
-            const size_t rows_all = (size_t)p.n * p.hq;
-            const size_t wrow = (size_t)split * rows_all + prow;
-            float4* dst = reinterpret_cast<float4*>(p.ws + wrow * D);
-#pragma unroll
-            for (int q = 0; q < D / 4; ++q)
-              dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-            float* wm = p.ws + (size_t)p.splits * rows_all * D;
-            wm[wrow] = (m_used == -INFINITY) ? -INFINITY : m_used * c;
-            wm[(size_t)p.splits * rows_all + wrow] = l;
+          p.ws[(size_t)split * rows_all + prow] =
+              l > 0.f ? m_used * c + __log2f(l) : -INFINITY;
+        }
+      }
+      ptx::mbar_arrive(bars.epi(t));
+      if (wait_bar(bars.epi(t), 0, abort_flag, p.dev_status)) {
+        uint8_t* dst_base = to_out ? reinterpret_cast<uint8_t*>(p.out)
+                                   : reinterpret_cast<uint8_t*>(p.ws) +
+                                         partial_o_offset(p.splits, rows_all) +
+                                         (size_t)split * rows_all * D * 2;
+        const int k0 = (sw & 7) * 32 + lane;  // 0..255 within the tile
+#pragma unroll 4
+        for (int idx = k0; idx < kBM * kChunks; idx += 2 * kBM) {
+          const int rl = idx / kChunks, ch = idx - rl * kChunks;
+          const int Rr = t * kBM + rl;
+          const int gr = row0 + Rr;
+          if (gr < p.rows_per_head) {
+            const int node = gr / G, jj = gr - node * G;
+            const size_t prow = (size_t)node * p.hq + (size_t)g * G + jj;
+            const uint4 v = *reinterpret_cast<const uint4*>(sm + L::kQ + (size_t)Rr * (D * 2) +
+                                                            ((ch + Rr) % kChunks) * 16);
+            *reinterpret_cast<uint4*>(dst_base + prow * (D * 2) + ch * 16) = v;
           }
         }
       }

@@ -41,9 +41,16 @@ bool use_tensor_cores(int32_t dtype);
 SplitPlan plan_attention(int32_t n, int32_t hq, int32_t hkv, int32_t d, int32_t dtype,
                          int32_t prefix, int sm_count);
 
-// Partials layout inside the workspace (fp32):
-//   acc [splits][n * hq][d], m [splits][n * hq], l [splits][n * hq]
-// row index n_i * hq + h.  m is the running maximum in log2 units.
+// Partials inside the workspace, for R = n * hq rows (row n_i * hq + h):
+//   lse [splits][R]  fp32: log2 of the split's softmax denominator, in the
+//                    log2-scaled score units (-inf when the split holds no
+//                    key the row may see)
+//   o   [splits][R][d]  the split's normalised output: fp32 for fp32
+//                    attention, fp16 for bf16 attention; starts at byte
+//                    partial_o_offset(splits, R)
+__host__ __device__ inline size_t partial_o_offset(int splits, size_t rows) {
+  return ((size_t)splits * rows * sizeof(float) + 255) & ~size_t(255);
+}
 cudaError_t launch_attn_simt(const AttnProblem& p, const SplitPlan& plan, float* ws,
                              cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnProblem& p, const SplitPlan& plan, float* ws,
