@@ -156,6 +156,39 @@ TV_API tv_status tv_tree_attn_verify(const void* q, const void* k_cache, const v
                               size_t ws_bytes, int32_t* dev_status, tv_stream_t stream);
 
 /*
+ * tv_tree_attn_verify_static -- tv_tree_attn_verify without a caller-passed
+ * workspace, for callers that cannot allocate device memory: code running
+ * inside a serving framework whose caching allocator owns all of the GPU's
+ * memory and forbids outside allocations, plug-ins that are only handed their
+ * input and output buffers, and latency-critical loops in which cudaMalloc or
+ * cudaFree would synchronise the device.  The paper has no counterpart; this
+ * is a convenience of this library.
+ *
+ * The split partials go to one scratch array of TV_STATIC_SCRATCH_BYTES
+ * (16 MiB) that the library defines in device memory; every GPU that loads
+ * the library holds it until the process exits.  The call allocates nothing
+ * and calls no allocating routine.  Arguments, layouts and results are those
+ * of tv_tree_attn_verify (minus workspace and ws_bytes).
+ *
+ *   - The first call on a device looks up the array's device address on that
+ *     device (with that device current); make that first call before any
+ *     stream capture.  Later calls reuse the cached address.
+ *   - A problem that needs more scratch than the array holds is rejected with
+ *     TV_ERR_CAPACITY before anything is launched (tv_attn_workspace_size
+ *     gives the bytes a problem needs).
+ *   - Every call shares the one array and it keeps the last call's contents;
+ *     nothing in it needs to start at zero, but two calls that overlap on the
+ *     GPU (different streams, or different host threads) race on it.
+ */
+#define TV_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+
+TV_API tv_status tv_tree_attn_verify_static(const void* q, const void* k_cache,
+                                            const void* v_cache, int64_t cap, int32_t prefix_len,
+                                            int32_t n_nodes, const int32_t* parent, void* out,
+                                            int32_t hq, int32_t hkv, int32_t d, int32_t dtype,
+                                            float scale, int32_t* dev_status, tv_stream_t stream);
+
+/*
  * tv_tree_accept -- greedy acceptance of the draft tree and the re-root map.
  *
  * Passage: SwiftSpec review page, "What carries the argument" (the tree

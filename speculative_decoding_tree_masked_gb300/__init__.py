@@ -122,6 +122,30 @@ def tree_attn_verify(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
     return out
 
 
+def tree_attn_verify_static(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            prefix_len: int, parent: torch.Tensor, out: torch.Tensor,
+                            scale: float = 0.0, status: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
+    """tree_attn_verify for callers that cannot allocate device memory: no
+    workspace is passed or allocated (the library's fixed 16 MiB device
+    scratch array holds the split partials) and `out` must be given.  Make
+    the first call on a device before any stream capture; calls that overlap
+    on the GPU share the scratch array and race."""
+    _need_cuda(q, k_cache, v_cache, parent, out)
+    n, hq, d = q.shape
+    hkv, cap, dk = k_cache.shape
+    if v_cache.shape != k_cache.shape or dk != d or parent.numel() != n or out.shape != q.shape:
+        raise ValueError("shape mismatch")
+    if k_cache.dtype != q.dtype or v_cache.dtype != q.dtype or out.dtype != q.dtype or \
+            parent.dtype != torch.int32:
+        raise ValueError("dtype mismatch")
+    _check(lib().tv_tree_attn_verify_static(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), cap, prefix_len, n, _ptr(parent), _ptr(out), hq,
+        hkv, d, _dtype_code(q), float(scale), _ptr(status), _stream(stream, q.device)),
+        "tv_tree_attn_verify_static")
+    return out
+
+
 def tree_accept(logits: torch.Tensor, token: torch.Tensor, parent: torch.Tensor, prefix_len: int,
                 outs: Optional[dict] = None, status: Optional[torch.Tensor] = None,
                 stream=None) -> dict:
