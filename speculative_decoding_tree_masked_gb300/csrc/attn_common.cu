@@ -95,7 +95,10 @@ __device__ __forceinline__ void load_partial(const __half* p, float (&o)[2]) {
 }
 
 // One warp per output row: O = sum_s 2^(lse_s - M) O_s / sum_s 2^(lse_s - M).
-template <typename PT, typename T, int D>
+// The merge is latency-bound: with the split count S known at compile time a
+// warp keeps all S partial loads in flight at once (one round trip for the
+// log-sum-exps, one for the partial rows); other split counts take the loop.
+template <typename PT, typename T, int D, int S>
 __global__ void __launch_bounds__(256) combine_kernel(const uint8_t* __restrict__ ws, int splits,
                                                       int rows, T* __restrict__ out) {
   constexpr int C = D / 32;  // consecutive columns per lane
@@ -104,22 +107,41 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint8_t* __restrict_
   if (row >= rows) return;
   const float* lse = reinterpret_cast<const float*>(ws);
   const PT* po = reinterpret_cast<const PT*>(ws + partial_o_offset(splits, rows));
-  float M = -INFINITY;
-#pragma unroll 4
-  for (int s = 0; s < splits; ++s) M = fmaxf(M, lse[(size_t)s * rows + row]);
   float W = 0.f;
   float o[C];
 #pragma unroll
   for (int c = 0; c < C; ++c) o[c] = 0.f;
-#pragma unroll 4
-  for (int s = 0; s < splits; ++s) {
-    const float ls = lse[(size_t)s * rows + row];
-    const float w = (ls == -INFINITY) ? 0.f : exp2f(ls - M);
-    W += w;
-    float x[C];
-    load_partial(po + ((size_t)s * rows + row) * D + lane * C, x);
+  if constexpr (S > 0) {
+    float ls[S], x[S][C];
 #pragma unroll
-    for (int c = 0; c < C; ++c) o[c] = fmaf(w, x[c], o[c]);
+    for (int s = 0; s < S; ++s) {
+      ls[s] = __ldg(lse + (size_t)s * rows + row);
+      load_partial(po + ((size_t)s * rows + row) * D + lane * C, x[s]);
+    }
+    float M = ls[0];
+#pragma unroll
+    for (int s = 1; s < S; ++s) M = fmaxf(M, ls[s]);
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+      const float w = (ls[s] == -INFINITY) ? 0.f : exp2f(ls[s] - M);
+      W += w;
+#pragma unroll
+      for (int c = 0; c < C; ++c) o[c] = fmaf(w, x[s][c], o[c]);
+    }
+  } else {
+    float M = -INFINITY;
+#pragma unroll 4
+    for (int s = 0; s < splits; ++s) M = fmaxf(M, lse[(size_t)s * rows + row]);
+#pragma unroll 4
+    for (int s = 0; s < splits; ++s) {
+      const float ls = lse[(size_t)s * rows + row];
+      const float w = (ls == -INFINITY) ? 0.f : exp2f(ls - M);
+      W += w;
+      float x[C];
+      load_partial(po + ((size_t)s * rows + row) * D + lane * C, x);
+#pragma unroll
+      for (int c = 0; c < C; ++c) o[c] = fmaf(w, x[c], o[c]);
+    }
   }
   const float inv = W > 0.f ? 1.f / W : 0.f;
   T* dst = out + (size_t)row * D + lane * C;
@@ -127,19 +149,37 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint8_t* __restrict_
   for (int c = 0; c < C; ++c) store_f32(dst + c, o[c] * inv);
 }
 
+template <typename PT, typename T, int D, int S>
+void launch_combine_s(const uint8_t* w, int splits, int rows, T* out, cudaStream_t s) {
+  combine_kernel<PT, T, D, S><<<(rows + 7) / 8, 256, 0, s>>>(w, splits, rows, out);
+}
+
+template <typename PT, typename T, int D>
+void launch_combine_d(const uint8_t* w, int splits, int rows, T* out, cudaStream_t s) {
+  switch (splits) {
+#define TV_COMBINE_CASE(n) \
+  case n: launch_combine_s<PT, T, D, n>(w, splits, rows, out, s); break;
+    TV_COMBINE_CASE(2) TV_COMBINE_CASE(3) TV_COMBINE_CASE(4) TV_COMBINE_CASE(5)
+    TV_COMBINE_CASE(6) TV_COMBINE_CASE(7) TV_COMBINE_CASE(8) TV_COMBINE_CASE(9)
+    TV_COMBINE_CASE(10) TV_COMBINE_CASE(11) TV_COMBINE_CASE(12)
+#undef TV_COMBINE_CASE
+    default: launch_combine_s<PT, T, D, 0>(w, splits, rows, out, s); break;
+  }
+}
+
 cudaError_t launch_combine(const AttnProblem& p, const SplitPlan& plan, const float* ws,
                            cudaStream_t s) {
   const int rows = p.n * p.hq;
-  const dim3 grid((rows + 7) / 8), block(256);
   const auto* w = reinterpret_cast<const uint8_t*>(ws);
   if (p.dtype == TV_BF16) {
     auto* out = static_cast<__nv_bfloat16*>(p.out);
-    if (p.d == 128) combine_kernel<__half, __nv_bfloat16, 128><<<grid, block, 0, s>>>(w, plan.splits, rows, out);
-    else combine_kernel<__half, __nv_bfloat16, 64><<<grid, block, 0, s>>>(w, plan.splits, rows, out);
+    if (p.d == 128) launch_combine_d<__half, __nv_bfloat16, 128>(w, plan.splits, rows, out, s);
+    else launch_combine_d<__half, __nv_bfloat16, 64>(w, plan.splits, rows, out, s);
   } else {
+    // the fp32 path is not latency-critical: one loop kernel
     auto* out = static_cast<float*>(p.out);
-    if (p.d == 128) combine_kernel<float, float, 128><<<grid, block, 0, s>>>(w, plan.splits, rows, out);
-    else combine_kernel<float, float, 64><<<grid, block, 0, s>>>(w, plan.splits, rows, out);
+    if (p.d == 128) launch_combine_s<float, float, 128, 0>(w, plan.splits, rows, out, s);
+    else launch_combine_s<float, float, 64, 0>(w, plan.splits, rows, out, s);
   }
   return cudaGetLastError();
 }

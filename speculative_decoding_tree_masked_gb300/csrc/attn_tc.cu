@@ -68,6 +68,7 @@ constexpr int kSoftmaxWarp0 = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr long long kWaitCycles = 4000000000LL;
+constexpr uint32_t kSleepHintNs = 20000;  // longest single hardware sleep of a wait
 
 struct TcParams {
   const __nv_bfloat16* q;
@@ -89,7 +90,7 @@ struct Layout {
   static constexpr uint32_t kPar = kV + kStages * kKV;
   static constexpr uint32_t kXch = kPar + kMaxNodes * 4;   // [tile][half][row] floats
   static constexpr uint32_t kBar = kXch + kTiles * 2 * kBM * 4;
-  static constexpr uint32_t kNumBars = 3 * kTiles + 3 * kStages + kTiles * 4 + kTiles;
+  static constexpr uint32_t kNumBars = 3 * kTiles + 4 * kStages + kTiles * 4 + kTiles;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kMisc + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // slack to align the base to 1024
@@ -102,20 +103,22 @@ struct Bars {
   __device__ uint32_t o_final(int t) const { return base + 8 * (2 * kTiles + t); }
   __device__ uint32_t k_full(int s) const { return base + 8 * (3 * kTiles + s); }
   __device__ uint32_t v_full(int s) const { return base + 8 * (3 * kTiles + kStages + s); }
-  __device__ uint32_t kv_empty(int s) const { return base + 8 * (3 * kTiles + 2 * kStages + s); }
+  // the K (V) slot of stage s may be refilled: the last MMA reading it is done
+  __device__ uint32_t k_empty(int s) const { return base + 8 * (3 * kTiles + 2 * kStages + s); }
+  __device__ uint32_t v_empty(int s) const { return base + 8 * (3 * kTiles + 3 * kStages + s); }
   // exchange between the two softmax warps of one (tile, row quarter)
   __device__ uint32_t xchg(int t, int q) const {
-    return base + 8 * (3 * kTiles + 3 * kStages + 4 * t + q);
+    return base + 8 * (3 * kTiles + 4 * kStages + 4 * t + q);
   }
   // every softmax thread of tile t has staged its output row
-  __device__ uint32_t epi(int t) const { return base + 8 * (7 * kTiles + 3 * kStages + t); }
+  __device__ uint32_t epi(int t) const { return base + 8 * (7 * kTiles + 4 * kStages + t); }
 };
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          int32_t* dev_status) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!ptx::mbar_try_wait(bar, parity)) {
+  while (!ptx::mbar_try_wait_sleep(bar, parity, kSleepHintNs)) {
     if (*abort_flag) return false;
     if (clock64() - t0 > kWaitCycles) {
       *abort_flag = 1;
@@ -198,7 +201,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(bars.k_full(s), 1);
       ptx::mbar_init(bars.v_full(s), 1);
-      ptx::mbar_init(bars.kv_empty(s), 1);
+      ptx::mbar_init(bars.k_empty(s), 1);
+      ptx::mbar_init(bars.v_empty(s), 1);
     }
     for (int t = 0; t < kTiles; ++t) {
       for (int q = 0; q < 4; ++q) ptx::mbar_init(bars.xchg(t, q), 64);
@@ -209,24 +213,29 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   }
   // The producer thread (tid 0) starts streaming K/V at once: the first
   // kStages blocks need no free slot and do not depend on Q.
-  auto load_block = [&](int j) {
+  auto load_k = [&](int j) {
     const int s = j % kStages;
-    const int key0 = kbeg + j * kBN;
     ptx::mbar_arrive_expect_tx(bars.k_full(s), L::kKV);
 #pragma unroll
     for (int c = 0; c < D / 64; ++c)
       ptx::tma_load_3d(base + L::kK + s * L::kKV + c * (kBN * 128), &kmap, bars.k_full(s), c * 64,
-                       key0, g);
+                       kbeg + j * kBN, g);
+  };
+  auto load_v = [&](int j) {
+    const int s = j % kStages;
     ptx::mbar_arrive_expect_tx(bars.v_full(s), L::kKV);
 #pragma unroll
     for (int c = 0; c < D / 64; ++c)
       ptx::tma_load_3d(base + L::kV + s * L::kKV + c * (kBN * 128), &vmap, bars.v_full(s), c * 64,
-                       key0, g);
+                       kbeg + j * kBN, g);
   };
-  if (tid == 0 && nb > 0) load_block(0);
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
     ptx::tmem_relinquish();
+  }
+  if (tid == 0 && nb > 0) {
+    load_k(0);
+    load_v(0);
   }
   for (int i = tid; i < p.n; i += kThreads) par[i] = p.parent[i];
   {
@@ -276,15 +285,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      // block 1 is requested once block 0's keys have landed, so that the
-      // first block of every CTA reaches the SMs ahead of the rest
+      // Block 1 is requested once block 0's keys have landed, so that the
+      // first block of every CTA reaches the SMs ahead of the rest.  After
+      // that a K slot is refilled as soon as the last QK^T reading it is
+      // done and a V slot once the last PV reading it is done: keys run
+      // about half a block ahead of values.
       for (int j = 1; j < nb; ++j) {
         const int s = j % kStages, u = j / kStages;
-        const bool ready = j < kStages
-                               ? wait_bar(bars.k_full(0), 0, abort_flag, p.dev_status)
-                               : wait_bar(bars.kv_empty(s), (u - 1) & 1, abort_flag, p.dev_status);
+        bool ready = j < kStages ? wait_bar(bars.k_full(0), 0, abort_flag, p.dev_status)
+                                 : wait_bar(bars.k_empty(s), (u - 1) & 1, abort_flag, p.dev_status);
         if (!ready) break;
-        load_block(j);
+        load_k(j);
+        if (j >= kStages &&
+            !wait_bar(bars.v_empty(s), (u - 1) & 1, abort_flag, p.dev_status))
+          break;
+        load_v(j);
       }
     }
   } else if (warp == 1) {
@@ -292,27 +307,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     if (lane == 0) {
       constexpr uint32_t kIdescQK = ptx::idesc_bf16(kBM, kBN, false);
       constexpr uint32_t kIdescPV = ptx::idesc_bf16(kBM, D, true);
+      // Descriptors are built once; a K step only moves the start address
+      // (the low field, in 16-byte units), so each MMA issues in a couple of
+      // instructions.
+      const uint64_t q_desc = ptx::smem_desc_sw128(base + L::kQ, 16, 1024);
+      const uint64_t k_desc = ptx::smem_desc_sw128(base + L::kK, 16, 1024);
+      // V block, MN-major: 8-key groups 1024 B apart (SBO), the two 64-column
+      // halves of d kBN * 128 B apart (LBO)
+      const uint64_t v_desc = ptx::smem_desc_sw128(base + L::kV, kBN * 128, 1024);
       auto issue_qk = [&](int t, int s) {
-        const uint32_t qa = base + L::kQ + t * L::kQTile;
-        const uint32_t kb = base + L::kK + s * L::kKV;
+        const uint64_t qd = q_desc + ((t * L::kQTile) >> 4);
+        const uint64_t kd = k_desc + ((s * L::kKV) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t qo = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-          const uint32_t ko = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-          ptx::mma_ss(tmem + t * kBN, ptx::smem_desc_sw128(qa + qo, 16, 1024),
-                      ptx::smem_desc_sw128(kb + ko, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+          const uint32_t qo = ((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4;
+          const uint32_t ko = ((kk >> 2) * (kBN * 128) + (kk & 3) * 32) >> 4;
+          ptx::mma_ss(tmem + t * kBN, qd + qo, kd + ko, kIdescQK, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int t, int s, bool acc) {
-        const uint32_t vb = base + L::kV + s * L::kKV;
+        const uint64_t vd = v_desc + ((s * L::kKV) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          // V block, MN-major: 8-key groups 1024 B apart (SBO), the two
-          // 64-column halves of d kBN * 128 B apart (LBO)
-          ptx::mma_ts(tmem + 2 * kBN + t * D, tmem + t * kBN + kk * 8,
-                      ptx::smem_desc_sw128(vb + kk * 2048, kBN * 128, 1024), kIdescPV,
-                      (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          ptx::mma_ts(tmem + 2 * kBN + t * D, tmem + t * kBN + kk * 8, vd + ((kk * 2048) >> 4),
+                      kIdescPV, (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = nb > 0 && wait_bar(bars.k_full(0), 0, abort_flag, p.dev_status);
       if (ok) {
@@ -321,6 +339,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           issue_qk(t, 0);
           ptx::mma_commit(bars.s_full(t));
         }
+        ptx::mma_commit(bars.k_empty(0));
       }
       for (int j = 0; ok && j < nb; ++j) {
         const int s = j % kStages, u = j / kStages;
@@ -330,7 +349,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           if (!ok) break;
           ptx::tc_fence_after();
           issue_pv(t, s, j > 0);
-          if (t == ntiles - 1) ptx::mma_commit(bars.kv_empty(s));
+          if (t == ntiles - 1) ptx::mma_commit(bars.v_empty(s));
           if (j + 1 < nb) {
             const int s2 = (j + 1) % kStages, u2 = (j + 1) / kStages;
             if (t == 0) ok = wait_bar(bars.k_full(s2), u2 & 1, abort_flag, p.dev_status);
@@ -338,6 +357,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             ptx::tc_fence_after();
             issue_qk(t, s2);
             ptx::mma_commit(bars.s_full(t));
+            if (t == ntiles - 1) ptx::mma_commit(bars.k_empty(s2));
           } else {
             ptx::mma_commit(bars.o_final(t));
           }
