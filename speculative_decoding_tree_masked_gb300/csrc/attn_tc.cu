@@ -233,10 +233,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
     ptx::tmem_relinquish();
   }
-  if (tid == 0 && nb > 0) {
-    load_k(0);
-    load_v(0);
-  }
+  if (tid == 0 && nb > 0) load_k(0);  // V_0 follows once K_0 has landed
   for (int i = tid; i < p.n; i += kThreads) par[i] = p.parent[i];
   {
     // Q tiles into shared memory in the K-major 128-byte-swizzled layout:
@@ -285,14 +282,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      // Block 1 is requested once block 0's keys have landed, so that the
-      // first block of every CTA reaches the SMs ahead of the rest.  After
-      // that a K slot is refilled as soon as the last QK^T reading it is
-      // done and a V slot once the last PV reading it is done: keys run
-      // about half a block ahead of values.
+      // V_0 and block 1 are requested once K_0 has landed, so that the first
+      // QK^T of every CTA is fed ahead of everything else.  After that a K
+      // slot is refilled as soon as the last QK^T reading it is done and a V
+      // slot once the last PV reading it is done: keys run about half a
+      // block ahead of values.
+      if (nb > 0 && wait_bar(bars.k_full(0), 0, abort_flag, p.dev_status)) load_v(0);
       for (int j = 1; j < nb; ++j) {
         const int s = j % kStages, u = j / kStages;
-        bool ready = j < kStages ? wait_bar(bars.k_full(0), 0, abort_flag, p.dev_status)
+        bool ready = j < kStages ? true
                                  : wait_bar(bars.k_empty(s), (u - 1) & 1, abort_flag, p.dev_status);
         if (!ready) break;
         load_k(j);
