@@ -197,6 +197,24 @@ def _oracle_subprocess(nodes, layers, repeats):
     return json.loads(out.stdout.strip().splitlines()[-1])
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x (the slowest rank's time): an all-reduce
+    MAX over the default process group, or x itself on one rank."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, units_per_rank_step: int, steps: int, max_seconds: float) -> float:
+    """Whole-job rate: the units all ranks processed divided by the slowest
+    rank's time (replicas each do the same per-rank work: weak scaling)."""
+    return world * units_per_rank_step * steps / max_seconds
+
+
 def _line_base(args, n_gpus):
     return {
         "metric": "tree-verify tokens/s", "unit": "tree tokens/s", "n_gpus": n_gpus,
@@ -273,10 +291,7 @@ def _end_to_end(args, world, dev, stream, step, q, logits, token, parent, acc, w
             stream.synchronize()
             _ = int(res_h["m"][0])  # the host reads the result
     secs = time.perf_counter() - t0
-    te = torch.tensor([secs], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    return float(te.item()), h2d, d2h
+    return max_over_ranks(secs, world, dev), h2d, d2h
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -358,11 +373,7 @@ def run_gpu(args, rank, world, local_rank):
                 ev[i + 1].record(stream)
         barrier()
     per_step = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    total_ms = ev[0].elapsed_time(ev[-1])
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), world, dev)
 
     # the dominant kernel alone: every layer's attention call, events on its stream
     reps = max(3, args.steps)
@@ -420,12 +431,12 @@ def run_gpu(args, rank, world, local_rank):
         line["config"]["layers"] = layers
         line["config"]["workload"] += f" (profiling case: {layers} layers)"
     line.update({
-        "value": world * NODES * args.steps / (total_ms * 1e-3),
+        "value": job_throughput(world, NODES, args.steps, total_ms * 1e-3),
         "ms_per_step": ms,
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": None if e2e is None else {
-            "value": world * NODES * args.steps / e2e[0], "unit": "tree tokens/s",
+            "value": job_throughput(world, NODES, args.steps, e2e[0]), "unit": "tree tokens/s",
             "h2d_bytes_per_step": e2e[1], "d2h_bytes_per_step": e2e[2]},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(peaks["sm_max_mhz"]),
