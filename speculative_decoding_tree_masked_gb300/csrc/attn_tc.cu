@@ -49,6 +49,7 @@
 #include <cuda_fp16.h>
 
 #include <cmath>
+#include <cstring>
 
 #include "common.cuh"
 #include "internal.h"
@@ -77,6 +78,7 @@ struct TcParams {
   const int32_t* parent;
   int32_t* dev_status;
   int32_t n, hq, hkv, prefix, keys, keys_per_split, splits, rows_per_head;
+  int32_t q_tma;  // 1: Q tiles arrive by TMA (G divides 128), 0: threads gather them
   float scale_log2;
 };
 
@@ -90,7 +92,7 @@ struct Layout {
   static constexpr uint32_t kPar = kV + kStages * kKV;
   static constexpr uint32_t kXch = kPar + kMaxNodes * 4;   // [tile][half][row] floats
   static constexpr uint32_t kBar = kXch + kTiles * 2 * kBM * 4;
-  static constexpr uint32_t kNumBars = 3 * kTiles + 4 * kStages + kTiles * 4 + kTiles;
+  static constexpr uint32_t kNumBars = 3 * kTiles + 4 * kStages + kTiles * 4 + kTiles + 1;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kMisc + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // slack to align the base to 1024
@@ -112,6 +114,8 @@ struct Bars {
   }
   // every softmax thread of tile t has staged its output row
   __device__ uint32_t epi(int t) const { return base + 8 * (7 * kTiles + 4 * kStages + t); }
+  // the Q tiles have landed (TMA path)
+  __device__ uint32_t q_full() const { return base + 8 * (8 * kTiles + 4 * kStages); }
 };
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -171,7 +175,7 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-               const TcParams p) {
+               const __grid_constant__ CUtensorMap qmap, const TcParams p) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -208,6 +212,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       for (int q = 0; q < 4; ++q) ptx::mbar_init(bars.xchg(t, q), 64);
       ptx::mbar_init(bars.epi(t), 2 * kBM);
     }
+    ptx::mbar_init(bars.q_full(), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -233,9 +238,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
     ptx::tmem_relinquish();
   }
+  if (tid == 0 && p.q_tma) {
+    // A tile's 128 rows are 128/G consecutive nodes x the G query heads of
+    // KV head g: one box per 64-column chunk over Q seen as [N][Hq][d], in
+    // the 128-byte-swizzled K-major layout; nodes past the tree read as zero.
+    ptx::mbar_arrive_expect_tx(bars.q_full(), ntiles * L::kQTile);
+    for (int t = 0; t < ntiles; ++t)
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        ptx::tma_load_3d(base + L::kQ + t * L::kQTile + c * (kBM * 128), &qmap, bars.q_full(),
+                         c * 64, g * G, (row0 + t * kBM) / G);
+  }
   if (tid == 0 && nb > 0) load_k(0);  // V_0 follows once K_0 has landed
   for (int i = tid; i < p.n; i += kThreads) par[i] = p.parent[i];
-  {
+  if (!p.q_tma) {
     // Q tiles into shared memory in the K-major 128-byte-swizzled layout:
     // 64-element column chunks of [128 rows][128 B], the 16-byte piece c of
     // row r stored at piece position c ^ (r % 8).  All loads of a thread are
@@ -331,6 +347,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                       kIdescPV, (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = nb > 0 && wait_bar(bars.k_full(0), 0, abort_flag, p.dev_status);
+      if (ok && p.q_tma) ok = wait_bar(bars.q_full(), 0, abort_flag, p.dev_status);
       if (ok) {
         ptx::tc_fence_after();
         for (int t = 0; t < ntiles; ++t) {
@@ -579,6 +596,21 @@ bool make_kv_map(CUtensorMap* map, const void* base, int d, int rows, int64_t ca
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over Q [n][hq][d] (bf16): boxes of 64 columns x G heads x 128/G
+// nodes (one 128-row tile of a KV head's query group), 128-byte swizzle,
+// nodes past the tree read as zero.
+bool make_q_map(CUtensorMap* map, const void* base, int d, int n, int hq, int group) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hq, (cuuint64_t)n};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)hq * d * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)(kBM / group)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
 cudaError_t launch_d(const AttnProblem& p, const SplitPlan& plan, float* ws, cudaStream_t s) {
   static bool attr_set[64];
@@ -591,11 +623,15 @@ cudaError_t launch_d(const AttnProblem& p, const SplitPlan& plan, float* ws, cud
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  CUtensorMap kmap, vmap;
+  CUtensorMap kmap, vmap, qmap;
   const int rows = p.prefix + p.n;
   if (!make_kv_map(&kmap, p.k, D, rows, p.cap, p.hkv) ||
       !make_kv_map(&vmap, p.v, D, rows, p.cap, p.hkv))
     return cudaErrorInvalidValue;
+  const int group = p.hq / p.hkv;
+  const bool q_tma = (kBM % group) == 0;
+  if (q_tma && !make_q_map(&qmap, p.q, D, p.n, p.hq, group)) return cudaErrorInvalidValue;
+  if (!q_tma) memset(&qmap, 0, sizeof(qmap));
   TcParams tp{};
   tp.q = static_cast<const __nv_bfloat16*>(p.q);
   tp.out = static_cast<__nv_bfloat16*>(p.out);
@@ -611,8 +647,9 @@ cudaError_t launch_d(const AttnProblem& p, const SplitPlan& plan, float* ws, cud
   tp.splits = plan.splits;
   tp.rows_per_head = (p.hq / p.hkv) * p.n;
   tp.scale_log2 = p.scale_log2;
+  tp.q_tma = q_tma ? 1 : 0;
   const dim3 grid(plan.splits, plan.row_tiles, p.hkv);
-  attn_tc_kernel<D><<<grid, kThreads, Layout<D>::kAlloc, s>>>(kmap, vmap, tp);
+  attn_tc_kernel<D><<<grid, kThreads, Layout<D>::kAlloc, s>>>(kmap, vmap, qmap, tp);
   return cudaGetLastError();
 }
 
