@@ -175,7 +175,8 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-               const __grid_constant__ CUtensorMap qmap, const TcParams p) {
+               const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+               const TcParams p) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -526,9 +527,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             w[e] = to_out ? pack_bf16x2(a, b) : pack_f16x2(a, b);
           }
           const int k = h * (kChunks / 2) + q;
-          *reinterpret_cast<uint4*>(srow + ((k + R) % kChunks) * 16) =
-              make_uint4(w[0], w[1], w[2], w[3]);
+          if (p.q_tma) {
+            // the TMA store's layout: 64-column chunks of [128 rows][128 B],
+            // 16-byte piece c of row r at piece position c ^ (r % 8)
+            const uint32_t off = L::kQ + t * L::kQTile + (k >> 3) * (kBM * 128) + r * 128 +
+                                 (((k & 7) ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(sm + off) = make_uint4(w[0], w[1], w[2], w[3]);
+          } else {
+            *reinterpret_cast<uint4*>(srow + ((k + R) % kChunks) * 16) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
         }
+        if (p.q_tma) ptx::fence_proxy_async_smem();
         if (!to_out && h == 0 && row_ok) {
           const int node = grow / G, jj = grow - node * G;
           const size_t prow = (size_t)node * p.hq + (size_t)g * G + jj;
@@ -537,7 +547,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         }
       }
       ptx::mbar_arrive(bars.epi(t));
-      if (wait_bar(bars.epi(t), 0, abort_flag, p.dev_status)) {
+      if (p.q_tma) {
+        // one thread of the tile writes it with tensor-map stores: a box of
+        // 64 columns x G heads x 128/G nodes per chunk, nodes past the tree
+        // clipped by the map
+        if ((sw & 7) == 0 && lane == 0 &&
+            wait_bar(bars.epi(t), 0, abort_flag, p.dev_status)) {
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            ptx::tma_store_4d(&omap, base + L::kQ + t * L::kQTile + c * (kBM * 128), c * 64,
+                              g * G, (row0 + t * kBM) / G, to_out ? 0 : split);
+          ptx::bulk_commit_group();
+          ptx::bulk_wait_group_read0();
+        }
+      } else if (wait_bar(bars.epi(t), 0, abort_flag, p.dev_status)) {
         uint8_t* dst_base = to_out ? reinterpret_cast<uint8_t*>(p.out)
                                    : reinterpret_cast<uint8_t*>(p.ws) +
                                          partial_o_offset(p.splits, rows_all) +
@@ -599,6 +622,23 @@ bool make_kv_map(CUtensorMap* map, const void* base, int d, int rows, int64_t ca
 // 3-D map over Q [n][hq][d] (bf16): boxes of 64 columns x G heads x 128/G
 // nodes (one 128-row tile of a KV head's query group), 128-byte swizzle,
 // nodes past the tree read as zero.
+// 4-D map over an output-shaped array [layers][n][hq][d] of 16-bit values
+// (the fp16 split partials, or the bf16 output with one layer): boxes of 64
+// columns x G heads x 128/G nodes x 1, no swizzle change from the Q tiles.
+bool make_o_map(CUtensorMap* map, void* base, bool fp16, int d, int n, int hq, int group,
+                int layers) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)hq, (cuuint64_t)n, (cuuint64_t)layers};
+  const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)hq * d * 2,
+                                 (cuuint64_t)n * hq * d * 2};
+  const cuuint32_t box[4] = {64, (cuuint32_t)group, (cuuint32_t)(kBM / group), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base,
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_q_map(CUtensorMap* map, const void* base, int d, int n, int hq, int group) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
@@ -623,7 +663,7 @@ cudaError_t launch_d(const AttnProblem& p, const SplitPlan& plan, float* ws, cud
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  CUtensorMap kmap, vmap, qmap;
+  CUtensorMap kmap, vmap, qmap, omap;
   const int rows = p.prefix + p.n;
   if (!make_kv_map(&kmap, p.k, D, rows, p.cap, p.hkv) ||
       !make_kv_map(&vmap, p.v, D, rows, p.cap, p.hkv))
@@ -632,6 +672,16 @@ cudaError_t launch_d(const AttnProblem& p, const SplitPlan& plan, float* ws, cud
   const bool q_tma = (kBM % group) == 0;
   if (q_tma && !make_q_map(&qmap, p.q, D, p.n, p.hq, group)) return cudaErrorInvalidValue;
   if (!q_tma) memset(&qmap, 0, sizeof(qmap));
+  if (q_tma) {
+    const bool to_out = plan.splits == 1;
+    void* obase = to_out ? p.out
+                         : static_cast<void*>(reinterpret_cast<uint8_t*>(ws) +
+                                              partial_o_offset(plan.splits, (size_t)p.n * p.hq));
+    if (!make_o_map(&omap, obase, !to_out, D, p.n, p.hq, group, to_out ? 1 : plan.splits))
+      return cudaErrorInvalidValue;
+  } else {
+    memset(&omap, 0, sizeof(omap));
+  }
   TcParams tp{};
   tp.q = static_cast<const __nv_bfloat16*>(p.q);
   tp.out = static_cast<__nv_bfloat16*>(p.out);
@@ -649,7 +699,7 @@ cudaError_t launch_d(const AttnProblem& p, const SplitPlan& plan, float* ws, cud
   tp.scale_log2 = p.scale_log2;
   tp.q_tma = q_tma ? 1 : 0;
   const dim3 grid(plan.splits, plan.row_tiles, p.hkv);
-  attn_tc_kernel<D><<<grid, kThreads, Layout<D>::kAlloc, s>>>(kmap, vmap, qmap, tp);
+  attn_tc_kernel<D><<<grid, kThreads, Layout<D>::kAlloc, s>>>(kmap, vmap, qmap, omap, tp);
   return cudaGetLastError();
 }
 
