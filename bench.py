@@ -41,6 +41,27 @@ def _algorithmic_work(parent, prefix, n, hq, hkv, d, elem=2):
     return bytes_, flops
 
 
+def _visible_pairs(parent, prefix, hq):
+    """(query row, key) pairs the mask lets through: one exponential each."""
+    from workloads import synth
+    n = len(parent)
+    return hq * (n * prefix + int((synth.node_depths(parent) + 1).sum()))
+
+
+MUFU_EX2_PER_CLK_SM = 16  # ex2 results per clock per SM (special-function units)
+SMS = 152
+
+
+def _bounds_us(nbytes, flops, exps, peaks):
+    """Lower bounds on one attention call's time (us): HBM bytes at the
+    measured copy bandwidth, flops at the measured bf16 rate, and one ex2 per
+    visible (row, key) pair on the special-function units at the maximum
+    SM clock."""
+    return {"hbm": nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6,
+            "tensor": flops / (peaks["bf16_tflops"] * 1e12) * 1e6,
+            "exp": exps / (MUFU_EX2_PER_CLK_SM * SMS * peaks["sm_max_mhz"] * 1e6) * 1e6}
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -401,6 +422,7 @@ def run_gpu(args, rank, world, local_rank):
     peaks = _peaks()
     nbytes, flops = _algorithmic_work(w.parent, PREFIX, NODES, HQ, HKV, D)
     t_layer = attn_ms_layer * 1e-3
+    bounds = _bounds_us(nbytes, flops, _visible_pairs(w.parent, PREFIX, HQ), peaks)
     gbs = nbytes / t_layer / 1e9
     tflops = flops / t_layer / 1e12
     tensor_path = tvp.lib().tv_attn_uses_tensor_cores(tvp.TV_BF16) == 1
@@ -445,9 +467,93 @@ def run_gpu(args, rank, world, local_rank):
         "step_ms_p10_p50_p90": [float(np.percentile(per_step, p)) for p in (10, 50, 90)],
         "attention": {"us_per_layer": attn_ms_layer * 1e3, "hbm_gbs": gbs,
                       "hbm_frac": gbs / peaks["hbm_gbs"], "tflops": tflops,
-                      "tensor_frac": tflops / peaks["bf16_tflops"]},
+                      "tensor_frac": tflops / peaks["bf16_tflops"],
+                      "bounds_us": bounds, "binding_frac": max(bounds.values()) /
+                      (attn_ms_layer * 1e3)},
     })
     print(json.dumps(line), flush=True)
+
+
+SWEEP_PREFIXES = (1024, 4096, 16384, 32768)
+SWEEP_NODES = (8, 32, 64, 128)
+
+
+def run_sweep(args, local_rank):
+    """Attention alone over the context/tree sweep at Qwen2-72B-class shapes
+    (64/8 heads, d128, bf16, random-parent trees of depth <= 16): one JSON
+    line per (prefix, nodes).  Each configuration cycles through enough
+    device copies of its KV cache that they exceed L2 several times over, in
+    a CUDA graph timed with events on its stream."""
+    import torch
+
+    import speculative_decoding_tree_masked_gb300 as tvp
+    from workloads import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.Stream(dev)
+    peaks = _peaks()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    nmax = max(SWEEP_NODES)
+    for prefix in SWEEP_PREFIXES:
+        big = synth.make_workload("q2_72b", seed=args.seed, prefix=prefix, n=nmax)
+        q_all, k0, v0 = synth.make_qkv(big, layer=0)
+        k0, v0 = k0.to(dev), v0.to(dev)
+        kv_bytes = 2 * k0.numel() * k0.element_size()
+        copies = int(min(96, max(3, -(-3 * 130_000_000 // kv_bytes))))
+        ks = [k0] + [k0.clone() for _ in range(copies - 1)]
+        vs = [v0] + [v0.clone() for _ in range(copies - 1)]
+        for n in SWEEP_NODES:
+            w = synth.make_workload("q2_72b", seed=args.seed, prefix=prefix, n=n)
+            q = q_all[:n].contiguous().to(dev)
+            parent = torch.from_numpy(w.parent).to(dev)
+            out = torch.empty_like(q)
+            ws = tvp.attn_workspace(n, w.hq, w.hkv, w.d, torch.bfloat16, prefix, dev)
+
+            def calls():
+                for c in range(copies):
+                    tvp.tree_attn_verify(q, ks[c], vs[c], prefix, parent, out=out, workspace=ws,
+                                         status=status)
+
+            with torch.cuda.stream(stream):
+                calls()
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                calls()
+            reps = max(3, int(2e5 / max(1, copies * prefix // 64)))
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    graph.replay()
+                ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                ea.record(stream)
+                for _ in range(reps):
+                    graph.replay()
+                eb.record(stream)
+            torch.cuda.synchronize()
+            if int(status.item()) != 0:
+                raise RuntimeError(f"device status {int(status.item())} in the sweep")
+            us = ea.elapsed_time(eb) * 1e3 / (reps * copies)
+            nbytes, flops = _algorithmic_work(w.parent, prefix, n, w.hq, w.hkv, w.d)
+            bounds = _bounds_us(nbytes, flops, _visible_pairs(w.parent, prefix, w.hq), peaks)
+            binding = max(bounds, key=bounds.get)
+            print(json.dumps({
+                "sweep": "tree attention, Qwen2-72B-class (64/8 heads, d128, bf16)",
+                "prefix": prefix, "tree_nodes": n, "depth": int(synth.node_depths(w.parent).max()),
+                "us_per_layer": us, "hbm_gbs": nbytes / us / 1e3,
+                "hbm_frac": nbytes / us / 1e3 / peaks["hbm_gbs"],
+                "tflops": flops / us / 1e6, "tensor_frac": flops / us / 1e6 / peaks["bf16_tflops"],
+                "bounds_us": bounds, "bound": binding, "binding_frac": bounds[binding] / us,
+                "splits": _splits_for(tvp, n, w.hq, w.hkv, w.d, prefix),
+                "kv_copies": copies, "peak_source": peaks["source"]}), flush=True)
+        del ks, vs, k0, v0
+        torch.cuda.empty_cache()
+
+
+def _splits_for(tvp, n, hq, hkv, d, prefix):
+    import torch
+    nbytes = tvp.attn_workspace_size(n, hq, hkv, d, torch.bfloat16, prefix)
+    return max(1, nbytes // (n * hq * (2 * d + 4)))
 
 
 def _attn_splits(tvp):
@@ -470,6 +576,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layers of KV per step (a smaller case for profiling)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the attention alone over the prefix x tree-size sweep "
+                         "(one JSON line per configuration) instead of the step")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -478,6 +587,10 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.sweep:
+        if rank == 0:
+            run_sweep(args, local_rank)
         return
     if world > 1:
         import torch

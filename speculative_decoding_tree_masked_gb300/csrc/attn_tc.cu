@@ -6,12 +6,13 @@
 // keys.  All rows of the group share every K/V block, so each block is
 // fetched once per CTA and multiplied against up to 256 rows.
 //
-// Warp roles (576 threads; every warp helps to load Q first):
+// Warp roles (320 threads; every warp helps to load Q first):
 //   warp 0      TMA producer: K and V blocks of 128 keys into a 2-stage ring
 //   warp 1      TMEM allocator and MMA issuer (one thread)
-//   warps 2-9   softmax of row tile 0, warps 10-17 of tile 1: two warps per
-//               32-row quarter, each on half of the key columns; a warp
-//               reaches the TMEM lanes 32 * (warp % 4) .. + 31, its rows
+//   warps 2-5   softmax of row tile 0, warps 6-9 of tile 1: one thread per
+//               query row; a warp reaches the TMEM lanes 32 * (warp % 4) ..
+//               + 31, which are its rows, so a row's maximum and sum never
+//               leave its thread
 //
 // Tensor memory (512 columns x 128 lanes of 32 bit):
 //   S_t  columns [128 t, 128 t + 128)   scores of tile t, fp32; the softmax
@@ -20,12 +21,12 @@
 //   O_t  columns [256 + D t, 256 + D t + D)   output accumulator of tile t
 //
 // Per key block j the MMA thread issues, for each tile t in turn,
-//   PV_t(j-1)  O_t += P_t . V        (A from TMEM, V from shared memory)
-//   QK_t(j)    S_t  = Q_t . K^T      (both from shared memory)
+//   PV_t(j)     O_t += P_t . V        (A from TMEM, V from shared memory)
+//   QK_t(j+1)   S_t  = Q_t . K^T      (both from shared memory)
 // so that while the softmax warps of one tile work, the tensor core runs the
 // other tile's products (ping-pong).  MMAs issued by one thread complete in
-// order, so S_t(j) being complete implies PV_t(j-1) is complete: the softmax
-// may then rescale O_t in place before releasing P_t(j).
+// order, so S_t(j+1) being complete implies PV_t(j) is complete: the softmax
+// may then rescale O_t in place before releasing P_t(j+1).
 //
 // Online softmax with a lazily moved maximum: the running maximum m used for
 // exponentiation is only raised when a block's maximum exceeds it by more
@@ -61,11 +62,12 @@ namespace {
 
 constexpr int kBM = 128;         // rows per tile (TMEM lanes)
 constexpr int kBN = 128;         // keys per block
-constexpr int kHalf = kBN / 2;   // key columns per softmax warp
+constexpr int kHalf = kBN / 2;   // key columns per TMEM load of the softmax
 constexpr int kTiles = 2;        // row tiles per CTA
 constexpr int kStages = 2;       // K/V ring depth
-constexpr int kThreads = 576;
+constexpr int kThreads = 320;
 constexpr int kSoftmaxWarp0 = 2;
+constexpr int kWarpsPerTile = 4;  // softmax warps of one row tile
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr long long kWaitCycles = 4000000000LL;
@@ -90,9 +92,8 @@ struct Layout {
   static constexpr uint32_t kK = kQ + kTiles * kQTile;
   static constexpr uint32_t kV = kK + kStages * kKV;
   static constexpr uint32_t kPar = kV + kStages * kKV;
-  static constexpr uint32_t kXch = kPar + kMaxNodes * 4;   // [tile][half][row] floats
-  static constexpr uint32_t kBar = kXch + kTiles * 2 * kBM * 4;
-  static constexpr uint32_t kNumBars = 3 * kTiles + 4 * kStages + kTiles * 4 + kTiles + 1;
+  static constexpr uint32_t kBar = kPar + kMaxNodes * 4;
+  static constexpr uint32_t kNumBars = 3 * kTiles + 4 * kStages + kTiles + 1;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kMisc + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // slack to align the base to 1024
@@ -108,14 +109,10 @@ struct Bars {
   // the K (V) slot of stage s may be refilled: the last MMA reading it is done
   __device__ uint32_t k_empty(int s) const { return base + 8 * (3 * kTiles + 2 * kStages + s); }
   __device__ uint32_t v_empty(int s) const { return base + 8 * (3 * kTiles + 3 * kStages + s); }
-  // exchange between the two softmax warps of one (tile, row quarter)
-  __device__ uint32_t xchg(int t, int q) const {
-    return base + 8 * (3 * kTiles + 4 * kStages + 4 * t + q);
-  }
   // every softmax thread of tile t has staged its output row
-  __device__ uint32_t epi(int t) const { return base + 8 * (7 * kTiles + 4 * kStages + t); }
+  __device__ uint32_t epi(int t) const { return base + 8 * (3 * kTiles + 4 * kStages + t); }
   // the Q tiles have landed (TMA path)
-  __device__ uint32_t q_full() const { return base + 8 * (8 * kTiles + 4 * kStages); }
+  __device__ uint32_t q_full() const { return base + 8 * (4 * kTiles + 4 * kStages); }
 };
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -200,7 +197,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   if (tid == 0) {
     for (int t = 0; t < kTiles; ++t) {
       ptx::mbar_init(bars.s_full(t), 1);
-      ptx::mbar_init(bars.p_full(t), 2 * kBM);
+      ptx::mbar_init(bars.p_full(t), kWarpsPerTile);
       ptx::mbar_init(bars.o_final(t), 1);
     }
     for (int s = 0; s < kStages; ++s) {
@@ -210,8 +207,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       ptx::mbar_init(bars.v_empty(s), 1);
     }
     for (int t = 0; t < kTiles; ++t) {
-      for (int q = 0; q < 4; ++q) ptx::mbar_init(bars.xchg(t, q), 64);
-      ptx::mbar_init(bars.epi(t), 2 * kBM);
+      ptx::mbar_init(bars.epi(t), kWarpsPerTile);
     }
     ptx::mbar_init(bars.q_full(), 1);
     *abort_flag = 0;
@@ -357,44 +353,51 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         }
         ptx::mma_commit(bars.k_empty(0));
       }
+      // The tensor pipe queues only a few MMAs, so any barrier query between
+      // two of them leaves it idle: the operand barriers are checked while
+      // the softmax still runs, and each tile's PV and QK^T then issue back
+      // to back.  Only a next key block that has not landed yet (a memory-
+      // bound case) is waited for between the two products.
       for (int j = 0; ok && j < nb; ++j) {
         const int s = j % kStages, u = j / kStages;
+        const bool more = j + 1 < nb;
+        const int s2 = (j + 1) % kStages, u2 = (j + 1) / kStages;
+        const bool k_ready = !more || ptx::mbar_test_wait(bars.k_full(s2), u2 & 1);
+        ok = wait_bar(bars.v_full(s), u & 1, abort_flag, p.dev_status);
         for (int t = 0; t < ntiles && ok; ++t) {
           ok = wait_bar(bars.p_full(t), j & 1, abort_flag, p.dev_status);
-          if (ok && t == 0) ok = wait_bar(bars.v_full(s), u & 1, abort_flag, p.dev_status);
           if (!ok) break;
           ptx::tc_fence_after();
           issue_pv(t, s, j > 0);
-          if (t == ntiles - 1) ptx::mma_commit(bars.v_empty(s));
-          if (j + 1 < nb) {
-            const int s2 = (j + 1) % kStages, u2 = (j + 1) / kStages;
-            if (t == 0) ok = wait_bar(bars.k_full(s2), u2 & 1, abort_flag, p.dev_status);
-            if (!ok) break;
-            ptx::tc_fence_after();
+          if (more) {
+            if (t == 0 && !k_ready) {
+              ok = wait_bar(bars.k_full(s2), u2 & 1, abort_flag, p.dev_status);
+              if (!ok) break;
+              ptx::tc_fence_after();
+            }
             issue_qk(t, s2);
             ptx::mma_commit(bars.s_full(t));
-            if (t == ntiles - 1) ptx::mma_commit(bars.k_empty(s2));
           } else {
             ptx::mma_commit(bars.o_final(t));
           }
+        }
+        if (ok) {
+          ptx::mma_commit(bars.v_empty(s));
+          if (more) ptx::mma_commit(bars.k_empty(s2));
         }
       }
     }
   } else if (warp >= kSoftmaxWarp0) {
     // ------------------------------------------------------------ softmax
-    // Two warps share each 32-row quarter of a tile: half h takes the key
-    // columns [64 h, 64 h + 64) of S and the output columns [D/2 h, D/2 (h+1))
-    // of O.  They trade partial row maxima (and finally row sums) through
-    // shared memory, synchronised by a 64-arrival mbarrier (bounded waits).
+    // One thread per query row: warp w of tile t reaches the TMEM lanes
+    // 32 (w % 4) .. + 31, so the row maximum and sum stay in the thread.
+    // Each block is read from TMEM twice (maximum, then exponentials), which
+    // keeps 64 scores live at a time.
     const int sw = warp - kSoftmaxWarp0;
-    const int t = sw >> 3;
-    const int h = (sw >> 2) & 1;
+    const int t = sw >> 2;
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;
     const int grow = row0 + t * kBM + r;
-    const uint32_t pair_bar = bars.xchg(t, quarter);
-    float* xch = reinterpret_cast<float*>(sm + L::kXch) + (t * 2 + h) * kBM;
-    const float* xch_other = reinterpret_cast<const float*>(sm + L::kXch) + (t * 2 + (1 - h)) * kBM;
     if (t < ntiles) {
       const bool row_ok = grow < p.rows_per_head;
       uint32_t anc[kMaskWords];
@@ -403,7 +406,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       if (row_ok && !ancestor_bits(par, grow / G, anc)) report(p.dev_status, TV_ERR_INVALID_TREE);
       const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
       const uint32_t t_s = tmem + lane_base + t * kBN;
-      const uint32_t t_o = tmem + lane_base + 2 * kBN + t * D + h * (D / 2);
+      const uint32_t t_o = tmem + lane_base + 2 * kBN + t * D;
       const float c = p.scale_log2;
       const float rescale_raw = kRescaleLog2 / c;
       float m_used = -INFINITY, l = 0.f;
@@ -412,34 +415,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         ok = wait_bar(bars.s_full(t), j & 1, abort_flag, p.dev_status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         ptx::tc_fence_after();
-        uint32_t sv[kHalf];
-        ptx::tmem_ld64(t_s + h * kHalf, sv);
-        ptx::tmem_wait_ld(sv);
-        float* s = reinterpret_cast<float*>(sv);
-        const int kb0 = kbeg + j * kBN + h * kHalf;
-        if (kb0 + kHalf > min(p.prefix, kend)) {
-#pragma unroll
-          for (int q = 0; q < kHalf / 32; ++q) {
-            const uint32_t vis = visible32(anc, p.prefix, kend, kb0 + 32 * q);
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (!((vis >> i) & 1u)) s[q * 32 + i] = -INFINITY;
-          }
-        }
+        const int kb0 = kbeg + j * kBN;
+        const bool edge = kb0 + kBN > min(p.prefix, kend);
         float mx[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = s[i];
+        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
 #pragma unroll
-        for (int i = 8; i < kHalf; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
-        const float pm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t sv[kHalf];
+          ptx::tmem_ld64(t_s + hh * kHalf, sv);
+          ptx::tmem_wait_ld(sv);
+          float* sc = reinterpret_cast<float*>(sv);
+          if (edge) {
+#pragma unroll
+            for (int q = 0; q < kHalf / 32; ++q) {
+              const uint32_t vis = visible32(anc, p.prefix, kend, kb0 + hh * kHalf + 32 * q);
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (!((vis >> i) & 1u)) sc[q * 32 + i] = -INFINITY;
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < kHalf; ++i) mx[i & 7] = fmaxf(mx[i & 7], sc[i]);
+        }
+        const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-        // both halves must have read S before either overwrites it with P,
-        // and need each other's maximum: one barrier does both
-        xch[r] = pm;
-        ptx::mbar_arrive(pair_bar);
-        ok = wait_bar(pair_bar, j & 1, abort_flag, p.dev_status);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        const float mb = fmaxf(pm, xch_other[r]);
         const float m_new = fmaxf(m_used, mb);
         const bool raise = m_new > m_used + rescale_raw;
         float alpha = 1.f;
@@ -449,25 +449,44 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         }
         const float mc = (m_used == -INFINITY) ? 0.f : m_used * c;
         float sum0 = 0.f, sum1 = 0.f;
+        // P (bf16 pairs) overwrites the first 64 columns of S: the scores of
+        // keys [64 hh, 64 hh + 64) go to columns [32 hh, 32 hh + 32), which
+        // this thread has already read in this pass
 #pragma unroll
-        for (int q = 0; q < kHalf / 32; ++q) {
-          uint32_t pk[16];
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t sv[kHalf];
+          ptx::tmem_ld64(t_s + hh * kHalf, sv);
+          ptx::tmem_wait_ld(sv);
+          float* sc = reinterpret_cast<float*>(sv);
+          if (edge) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float a = ptx::ex2(fmaf(s[q * 32 + 2 * i], c, -mc));
-            const float b = ptx::ex2(fmaf(s[q * 32 + 2 * i + 1], c, -mc));
-            sum0 += a;
-            sum1 += b;
-            pk[i] = pack_bf16x2(a, b);
+            for (int q = 0; q < kHalf / 32; ++q) {
+              const uint32_t vis = visible32(anc, p.prefix, kend, kb0 + hh * kHalf + 32 * q);
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (!((vis >> i) & 1u)) sc[q * 32 + i] = -INFINITY;
+            }
           }
-          ptx::tmem_st16(t_s + h * (kHalf / 2) + q * 16, pk);
+#pragma unroll
+          for (int q = 0; q < kHalf / 32; ++q) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float a = ptx::ex2(fmaf(sc[q * 32 + 2 * i], c, -mc));
+              const float b = ptx::ex2(fmaf(sc[q * 32 + 2 * i + 1], c, -mc));
+              sum0 += a;
+              sum1 += b;
+              pk[i] = pack_bf16x2(a, b);
+            }
+            ptx::tmem_st16(t_s + hh * (kHalf / 2) + q * 16, pk);
+          }
         }
         l = l * alpha + (sum0 + sum1);
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
           // O_t holds the sum through block j-1 (complete, see above) and
           // PV_t(j) waits for this thread's P_full arrival
 #pragma unroll
-          for (int q = 0; q < D / 64; ++q) {
+          for (int q = 0; q < D / 32; ++q) {
             uint32_t v[32];
             ptx::tmem_ld32(t_o + q * 32, v);
             ptx::tmem_wait_ld(v);
@@ -478,84 +497,71 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bars.p_full(t));
-        // the next block's exchange slot is written only after the partner
-        // has read this one: the partner's read precedes its P_full arrival,
-        // and this thread's next write follows the next S_full wait, which
-        // needs every arrival
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bars.p_full(t));
       }
       // epilogue: O_t is final once the last PV has completed
       if (ok) ok = wait_bar(bars.o_final(t), 0, abort_flag, p.dev_status);
-      // row sum = the two halves' sums (same m_used in both); the partner
-      // read this slot's last maximum before its final P_full arrival, which
-      // the final PV (and so o_final) waited for
-      if (ok) {
-        xch[r] = l;
-        ptx::mbar_arrive(pair_bar);
-        ok = wait_bar(pair_bar, nb & 1, abort_flag, p.dev_status);
-        l += xch_other[r];
-      }
-      // Stage this thread's normalised half-row as 16-bit values in shared
-      // memory (the Q tiles are free: every MMA has completed), then copy the
-      // tile out with coalesced 16-byte stores.  Row R's 16-byte chunk k sits
-      // at chunk position (k + R) % kChunks, which spreads a warp's stores
-      // over all banks.  With one split the result is the final bf16 output;
-      // otherwise it is the split's fp16 partial plus its log-sum-exp.
+      // Stage this thread's normalised row as 16-bit values in shared memory
+      // (the Q tiles are free: every MMA has completed), then copy the tile
+      // out.  With one split the result is the final bf16 output; otherwise
+      // it is the split's fp16 partial plus its log-sum-exp.
       constexpr int kChunks = D / 8;
       const bool to_out = p.splits == 1;
       const size_t rows_all = (size_t)p.n * p.hq;
       const int R = t * kBM + r;
       if (__all_sync(0xffffffffu, ok)) {
         ptx::tc_fence_after();
-        float o[D / 2];
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint8_t* srow = sm + L::kQ + (size_t)R * (D * 2);
 #pragma unroll
-        for (int q = 0; q < D / 64; ++q) {
+        for (int q = 0; q < D / 32; ++q) {
           uint32_t v[32];
           ptx::tmem_ld32(t_o + q * 32, v);
           ptx::tmem_wait_ld(v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[q * 32 + i] = __uint_as_float(v[i]);
-        }
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        uint8_t* srow = sm + L::kQ + (size_t)R * (D * 2);
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t w[4];
 #pragma unroll
-        for (int q = 0; q < kChunks / 2; ++q) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float a = o[8 * q + 2 * e] * inv, b = o[8 * q + 2 * e + 1] * inv;
-            w[e] = to_out ? pack_bf16x2(a, b) : pack_f16x2(a, b);
-          }
-          const int k = h * (kChunks / 2) + q;
-          if (p.q_tma) {
-            // the TMA store's layout: 64-column chunks of [128 rows][128 B],
-            // 16-byte piece c of row r at piece position c ^ (r % 8)
-            const uint32_t off = L::kQ + t * L::kQTile + (k >> 3) * (kBM * 128) + r * 128 +
-                                 (((k & 7) ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4*>(sm + off) = make_uint4(w[0], w[1], w[2], w[3]);
-          } else {
-            *reinterpret_cast<uint4*>(srow + ((k + R) % kChunks) * 16) =
-                make_uint4(w[0], w[1], w[2], w[3]);
+            for (int e = 0; e < 4; ++e) {
+              const float a = __uint_as_float(v[8 * cc + 2 * e]) * inv;
+              const float b = __uint_as_float(v[8 * cc + 2 * e + 1]) * inv;
+              w[e] = to_out ? pack_bf16x2(a, b) : pack_f16x2(a, b);
+            }
+            const int k = q * 4 + cc;  // 16-byte chunk of the row
+            if (p.q_tma) {
+              // the TMA store's layout: 64-column chunks of [128 rows][128 B],
+              // 16-byte piece c of row r at piece position c ^ (r % 8)
+              const uint32_t off = L::kQ + t * L::kQTile + (k >> 3) * (kBM * 128) + r * 128 +
+                                   (((k & 7) ^ (r & 7)) << 4);
+              *reinterpret_cast<uint4*>(sm + off) = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+              // row R's chunk k at chunk position (k + R) % kChunks spreads a
+              // warp's stores over all banks
+              *reinterpret_cast<uint4*>(srow + ((k + R) % kChunks) * 16) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
+            }
           }
         }
         if (p.q_tma) ptx::fence_proxy_async_smem();
-        if (!to_out && h == 0 && row_ok) {
+        if (!to_out && row_ok) {
           const int node = grow / G, jj = grow - node * G;
           const size_t prow = (size_t)node * p.hq + (size_t)g * G + jj;
           p.ws[(size_t)split * rows_all + prow] =
               l > 0.f ? m_used * c + __log2f(l) : -INFINITY;
         }
       }
-      ptx::mbar_arrive(bars.epi(t));
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bars.epi(t));
       if (p.q_tma) {
         // one thread of the tile writes it with tensor-map stores: a box of
         // 64 columns x G heads x 128/G nodes per chunk, nodes past the tree
         // clipped by the map
-        if ((sw & 7) == 0 && lane == 0 &&
+        if ((sw & 3) == 0 && lane == 0 &&
             wait_bar(bars.epi(t), 0, abort_flag, p.dev_status)) {
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            ptx::tma_store_4d(&omap, base + L::kQ + t * L::kQTile + c * (kBM * 128), c * 64,
+          for (int cc = 0; cc < D / 64; ++cc)
+            ptx::tma_store_4d(&omap, base + L::kQ + t * L::kQTile + cc * (kBM * 128), cc * 64,
                               g * G, (row0 + t * kBM) / G, to_out ? 0 : split);
           ptx::bulk_commit_group();
           ptx::bulk_wait_group_read0();
@@ -565,9 +571,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                                    : reinterpret_cast<uint8_t*>(p.ws) +
                                          partial_o_offset(p.splits, rows_all) +
                                          (size_t)split * rows_all * D * 2;
-        const int k0 = (sw & 7) * 32 + lane;  // 0..255 within the tile
+        const int k0 = (sw & 3) * 32 + lane;  // 0..127 within the tile
 #pragma unroll 4
-        for (int idx = k0; idx < kBM * kChunks; idx += 2 * kBM) {
+        for (int idx = k0; idx < kBM * kChunks; idx += kBM) {
           const int rl = idx / kChunks, ch = idx - rl * kChunks;
           const int Rr = t * kBM + rl;
           const int gr = row0 + Rr;
