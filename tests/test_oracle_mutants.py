@@ -135,3 +135,94 @@ def test_last_occurrence_argmax_is_caught(monkeypatch):
         return (x.shape[1] - 1 - np.argmax(x[:, ::-1], axis=1)).astype(np.int32)
     monkeypatch.setattr(acc.oracle, "target_argmax", mutant)
     assert _fails(acc.test_argmax_ties_and_nan_follow_first_occurrence)
+
+
+# ------------------------------------------------------------ draft side
+
+import oracle.tree_expand as te  # noqa: E402
+from tests import test_oracle_expand as exp  # noqa: E402
+
+
+def _expand_pins():
+    return [
+        exp.check_worked_expansion,
+        lambda: exp.check_brute_force_by_probability(0),
+        lambda: exp.check_brute_force_by_probability(1),
+        lambda: exp.check_single_root_is_argmax(0),
+        exp.check_ties_go_to_lower_position_then_token,
+    ]
+
+
+def _reroot_pins():
+    return [lambda: exp.check_worked_reroot(c) for c in "ABC"]
+
+
+def test_draft_pins_pass_unmutated():
+    assert not _some_fail(_expand_pins())
+    assert not _some_fail(_reroot_pins())
+
+
+def test_expansion_without_path_score_is_caught(monkeypatch):
+    monkeypatch.setattr(te, "candidate_scores",
+                        lambda logits, frontier, cum: te.log_softmax(logits))
+    assert _some_fail(_expand_pins())
+
+
+def test_expansion_on_probabilities_is_caught(monkeypatch):
+    def prob_scores(logits, frontier, cum):
+        base = np.array([float(cum[int(u)]) for u in frontier])
+        return base[:, None] + np.exp(te.log_softmax(logits))
+    monkeypatch.setattr(te, "candidate_scores", prob_scores)
+    assert _some_fail(_expand_pins())
+
+
+def test_reversed_tie_rule_is_caught(monkeypatch):
+    def ml_expand_high_token_first(logits, frontier, cum, w):
+        scores = te.candidate_scores(logits, frontier, cum)
+        nf, vocab = scores.shape
+        flat = scores.ravel()
+        order = np.lexsort((-np.arange(flat.size), -flat))[:w]
+        f, v = np.divmod(order, vocab)
+        parent = np.array([int(frontier[int(i)]) for i in f], dtype=np.int32)
+        return parent, v.astype(np.int32), flat[order]
+    monkeypatch.setattr(te, "ml_expand", ml_expand_high_token_first)
+    monkeypatch.setattr(exp.oracle, "ml_expand", ml_expand_high_token_first)
+    assert _some_fail(_expand_pins())
+
+
+def test_target_side_survivors_on_the_draft_side_are_caught(monkeypatch):
+    # the subtree under a_m itself (the target side's rule), bonus ignored
+    def strict_desc_rule(parent, token, cum, path, bonus, prefix_len):
+        n = len(parent)
+        path = [int(a) for a in path]
+        surv = [i for i in range(n) if i != path[-1]
+                and path[-1] in te.ancestors_inclusive(parent, i)]
+        new_pos = np.full(n, -1, dtype=np.int32)
+        for idx, node in enumerate(path + surv):
+            new_pos[node] = prefix_len + idx
+        rank = {node: k for k, node in enumerate(surv)}
+        new_parent = np.full(n, -1, dtype=np.int32)
+        new_token = np.full(n, -1, dtype=np.int32)
+        new_cum = np.zeros(n)
+        for k, node in enumerate(surv):
+            new_parent[k] = rank.get(int(parent[node]), -1)
+            new_token[k] = int(token[node])
+            new_cum[k] = float(cum[node]) - float(cum[path[-1]])
+        return {"new_pos": new_pos, "new_parent": new_parent, "new_token": new_token,
+                "new_cum": new_cum, "n_survivors": len(surv), "new_root": path[-1]}
+    monkeypatch.setattr(exp.oracle, "draft_reroot", strict_desc_rule)
+    assert _some_fail(_reroot_pins())
+
+
+def test_unrebased_path_scores_are_caught(monkeypatch):
+    orig = te.draft_reroot
+
+    def no_rebase(parent, token, cum, path, bonus, prefix_len):
+        res = orig(parent, token, cum, path, bonus, prefix_len)
+        r = res["n_survivors"]
+        if r:
+            b = res["new_root"]
+            res["new_cum"][:r] += float(cum[b])
+        return res
+    monkeypatch.setattr(exp.oracle, "draft_reroot", no_rebase)
+    assert _some_fail(_reroot_pins())
