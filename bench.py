@@ -550,6 +550,66 @@ def run_sweep(args, local_rank):
         torch.cuda.empty_cache()
 
 
+def run_expand(args, local_rank):
+    """The draft side alone, at the pages' width: one maximum-likelihood
+    expansion of w = 8 leaves from 8 frontier nodes over a 128256-token
+    vocabulary (float32 logits, 4.1 MB), cycling through enough copies of the
+    logits to exceed L2, then the draft re-root map.  One JSON line."""
+    import numpy as np
+    import torch
+
+    import speculative_decoding_tree_masked_gb300 as tvp
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.Stream(dev)
+    peaks = _peaks()
+    nf, w, vocab, n_nodes = 8, 8, VOCAB, 64
+    rng = np.random.default_rng(args.seed)
+    base = torch.from_numpy(rng.standard_normal((nf, vocab), dtype=np.float32) * 3).to(dev)
+    copies = max(3, -(-3 * 130_000_000 // (nf * vocab * 4)))
+    logits = [base] + [base.clone() for _ in range(copies - 1)]
+    frontier = torch.arange(n_nodes - nf, n_nodes, dtype=torch.int32, device=dev)
+    cum = torch.from_numpy(-rng.uniform(0, 6, size=n_nodes).astype(np.float32)).to(dev)
+    outs = {"parent": torch.empty(w, dtype=torch.int32, device=dev),
+            "token": torch.empty(w, dtype=torch.int32, device=dev),
+            "score": torch.empty(w, dtype=torch.float32, device=dev)}
+    ws = tvp.expand_workspace(nf, vocab, w, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def calls():
+        for c in range(copies):
+            tvp.tree_expand(logits[c], frontier, cum, w, outs=outs, workspace=ws, status=status)
+
+    with torch.cuda.stream(stream):
+        calls()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        calls()
+    reps = max(3, args.steps)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        eb.record(stream)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the expansion")
+    us = ea.elapsed_time(eb) * 1e3 / (reps * copies)
+    nbytes = nf * vocab * 4
+    print(json.dumps({
+        "kernel": "maximum-likelihood tree expansion (slice kernel + merge)",
+        "workload": f"{nf} frontier nodes x vocab {vocab} (float32 logits), w = {w}",
+        "us_per_call": us, "hbm_gbs": nbytes / us / 1e3,
+        "hbm_frac": nbytes / us / 1e3 / peaks["hbm_gbs"], "bytes": nbytes,
+        "l2": f"{copies} copies of the logits cycled (larger than L2)",
+        "peak_source": peaks["source"]}), flush=True)
+
+
 def _splits_for(tvp, n, hq, hkv, d, prefix):
     import torch
     nbytes = tvp.attn_workspace_size(n, hq, hkv, d, torch.bfloat16, prefix)
@@ -576,6 +636,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layers of KV per step (a smaller case for profiling)")
+    ap.add_argument("--expand", action="store_true",
+                    help="time the draft side's tree expansion instead of the step")
     ap.add_argument("--sweep", action="store_true",
                     help="time the attention alone over the prefix x tree-size sweep "
                          "(one JSON line per configuration) instead of the step")
@@ -588,9 +650,9 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
-    if args.sweep:
+    if args.sweep or args.expand:
         if rank == 0:
-            run_sweep(args, local_rank)
+            (run_sweep if args.sweep else run_expand)(args, local_rank)
         return
     if world > 1:
         import torch

@@ -265,6 +265,101 @@ TV_API tv_status tv_kv_compact(void* k_cache, void* v_cache, int32_t n_layers,
                         int32_t dtype, int32_t prefix_len, int32_t n_nodes,
                         const int32_t* new_pos, int32_t* dev_status, tv_stream_t stream);
 
+/*
+ * The draft side.  These two calls serve the draft model that proposes the
+ * trees; they are not part of the target's verification step.
+ */
+
+#define TV_MAX_EXPAND_WIDTH 64          /* w, new leaves per expansion */
+#define TV_MAX_EXPAND_CANDIDATES 1024   /* n_frontier * w, and ceil(vocab / 8192) * w */
+#define TV_MAX_VOCAB 524288
+
+/* Bytes of workspace tv_tree_expand needs; 0 for arguments it rejects. */
+TV_API size_t tv_expand_workspace_size(int32_t n_frontier, int32_t vocab, int32_t w);
+
+/*
+ * tv_tree_expand -- one maximum-likelihood expansion of the draft tree.
+ *
+ * Passage: SwiftSpec review page, "Assumptions & free parameters" (the
+ * domain assumption on maximum-likelihood tree expansion: a path scores the
+ * sum of the log-softmax probabilities along it, and the leaves to expand
+ * are chosen by that score; Algorithm 1 and Section 3.1 of the paper) and
+ * "Core claim".  The page gives the rule in prose; this library reads it as:
+ * every child (f, v) of a frontier node scores
+ *     cum[frontier[f]] + log_softmax(logits[f])[v]
+ * and the w best become new leaves, best first, equal scores going to the
+ * lower frontier position f and then to the lower token id v.
+ *
+ *   logits      device float32 [n_frontier][vocab]: the draft's logits at
+ *               each frontier node; finite or -inf (NaN is not supported).
+ *               A -inf logit's child scores -inf; a row that is -inf
+ *               throughout has no children
+ *   vocab       1 .. TV_MAX_VOCAB
+ *   n_frontier  1 .. TV_MAX_NODES
+ *   frontier    device int32 [n_frontier]: tree node of each logits row,
+ *               in [0, n_nodes)
+ *   cum         device float32 [n_nodes]: cumulative log-probability of
+ *               every tree node (0 at the root)
+ *   w           1 .. TV_MAX_EXPAND_WIDTH and at most n_frontier * vocab;
+ *               n_frontier * w and ceil(vocab / 8192) * w at most
+ *               TV_MAX_EXPAND_CANDIDATES (w = 64 allows a 131072-token
+ *               vocabulary, w = 16 the largest)
+ * Outputs (device, written; pass parent + N, token + N, cum + N to append
+ * the new leaves to a tree of N nodes):
+ *   new_parent  int32 [w]   tree node of each new leaf's parent
+ *   new_token   int32 [w]   its token
+ *   new_score   float32 [w] its cumulative log-probability (its score)
+ * workspace: device memory of at least tv_expand_workspace_size bytes; its
+ * contents on entry do not matter.  dev_status: device int32 or NULL;
+ * TV_ERR_INVALID_ARG when a frontier entry is out of range (the outputs are
+ * then -1 / -inf).  Scores are computed in float32, so candidates whose
+ * scores differ by less than float32 rounding may come out in either order.
+ */
+TV_API tv_status tv_tree_expand(const float* logits, int32_t vocab, int32_t n_frontier,
+                                const int32_t* frontier, const float* cum, int32_t n_nodes,
+                                int32_t w, int32_t* new_parent, int32_t* new_token,
+                                float* new_score, void* workspace, size_t ws_bytes,
+                                int32_t* dev_status, tv_stream_t stream);
+
+/*
+ * tv_draft_reroot -- the draft tree's re-root map after a verification.
+ *
+ * Passage: SwiftSpec review page, "What carries the argument" (after each
+ * verification the draft tree re-roots at the last verified token and the
+ * cache keeps only the still-useful subtree) and "Core claim".  The draft
+ * keeps expanding while the target verifies, so its tree extends the tree
+ * that was verified (the first nodes are the same).  This library reads the
+ * survivor rule as: the new root is the child b of the last accepted node
+ * a_m that carries the bonus token (the lowest-indexed one if several), and
+ * the survivors are b and its descendants, in node order; without such a
+ * child nothing survives.
+ *
+ *   parent, token  device int32 [n_nodes]: the draft tree (node 0 the root)
+ *   cum            device float32 [n_nodes]: cumulative log-probabilities
+ *   n_nodes        1 .. TV_MAX_NODES
+ *   path, m, out_tokens  device: the outputs of tv_tree_accept for the
+ *                  verified tree (path a_0..a_m, the bonus token out_tokens[m])
+ *   prefix_len     P, the prefix length before the verification
+ * Outputs (device, written):
+ *   new_pos      int32 [n_nodes]  cache row of each node's KV (old order):
+ *                a_k moves to row P + k, survivor k to row P + m + 1 + k,
+ *                others -1 (feed it to tv_kv_compact for the draft's cache)
+ *   new_parent   int32 [n_nodes]  parents of the survivors in their new order
+ *                (-1 for the new root b and for entries k >= r)
+ *   new_token    int32 [n_nodes]  their tokens (-1 for k >= r)
+ *   new_cum      float32 [n_nodes] their cumulative log-probabilities minus
+ *                that of b, so the new root has 0 (0 for k >= r)
+ *   n_survivors  int32 [1]        r
+ *   dev_status   device int32 or NULL; TV_ERR_INVALID_TREE on a bad parent,
+ *                m or path (outputs then -1 / 0, r = 0)
+ */
+TV_API tv_status tv_draft_reroot(const int32_t* parent, const int32_t* token, const float* cum,
+                                 int32_t n_nodes, const int32_t* path, const int32_t* m,
+                                 const int32_t* out_tokens, int32_t prefix_len,
+                                 int32_t* new_pos, int32_t* new_parent, int32_t* new_token,
+                                 float* new_cum, int32_t* n_survivors, int32_t* dev_status,
+                                 tv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

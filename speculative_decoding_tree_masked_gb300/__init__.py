@@ -188,3 +188,73 @@ def kv_compact(k_cache: torch.Tensor, v_cache: torch.Tensor, prefix_len: int, n_
         _ptr(k_cache), _ptr(v_cache), layers, hkv * cap * d, hkv, cap, d, _dtype_code(k_cache),
         prefix_len, n_nodes, _ptr(new_pos), _ptr(status), _stream(stream, k_cache.device)),
         "tv_kv_compact")
+
+
+# ---------------------------------------------------------------- draft side
+
+def expand_workspace(n_frontier: int, vocab: int, w: int, device) -> torch.Tensor:
+    """Workspace of tree_expand for these sizes (raises on sizes it rejects)."""
+    nbytes = int(lib().tv_expand_workspace_size(n_frontier, vocab, w))
+    if nbytes == 0:
+        raise TreeVerifyError(TV_ERR_INVALID_ARG, "tv_expand_workspace_size")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def tree_expand(logits: torch.Tensor, frontier: torch.Tensor, cum: torch.Tensor, w: int,
+                outs: Optional[dict] = None, workspace: Optional[torch.Tensor] = None,
+                status: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """One maximum-likelihood expansion: the w best children of the frontier
+    nodes by cumulative log-probability.  logits float32 [F][V] (row f for
+    tree node frontier[f]), frontier int32 [F], cum float32 [N] (every tree
+    node's cumulative log-probability).  Returns (or fills) a dict of device
+    tensors parent int32 [w], token int32 [w], score float32 [w]."""
+    _need_cuda(logits, frontier, cum)
+    nf, vocab = logits.shape
+    if logits.dtype != torch.float32 or cum.dtype != torch.float32 or \
+            frontier.dtype != torch.int32:
+        raise ValueError("dtype mismatch")
+    if frontier.numel() != nf or not logits.is_contiguous():
+        raise ValueError("shape mismatch")
+    if outs is None:
+        dev = logits.device
+        outs = {"parent": torch.empty(w, dtype=torch.int32, device=dev),
+                "token": torch.empty(w, dtype=torch.int32, device=dev),
+                "score": torch.empty(w, dtype=torch.float32, device=dev)}
+    if workspace is None:
+        workspace = expand_workspace(nf, vocab, w, logits.device)
+    _check(lib().tv_tree_expand(
+        _ptr(logits), vocab, nf, _ptr(frontier), _ptr(cum), cum.numel(), w, _ptr(outs["parent"]),
+        _ptr(outs["token"]), _ptr(outs["score"]), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(status),
+        _stream(stream, logits.device)), "tv_tree_expand")
+    return outs
+
+
+def draft_reroot(parent: torch.Tensor, token: torch.Tensor, cum: torch.Tensor, accepted: dict,
+                 prefix_len: int, outs: Optional[dict] = None,
+                 status: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """The draft tree's re-root map after a verification.  parent, token
+    int32 [N] and cum float32 [N] describe the draft tree; `accepted` is the
+    dict tree_accept returned for the verified tree (its path, m and
+    out_tokens are read on the device).  Returns a dict of device tensors
+    new_pos, new_parent, new_token (int32 [N]), new_cum (float32 [N]) and
+    n_survivors (int32 [1]); new_pos feeds kv_compact for the draft's cache."""
+    _need_cuda(parent, token, cum)
+    n = parent.numel()
+    if parent.dtype != torch.int32 or token.dtype != torch.int32 or cum.dtype != torch.float32:
+        raise ValueError("dtype mismatch")
+    if token.numel() != n or cum.numel() != n:
+        raise ValueError("shape mismatch")
+    if outs is None:
+        dev = parent.device
+        outs = {"new_pos": torch.empty(n, dtype=torch.int32, device=dev),
+                "new_parent": torch.empty(n, dtype=torch.int32, device=dev),
+                "new_token": torch.empty(n, dtype=torch.int32, device=dev),
+                "new_cum": torch.empty(n, dtype=torch.float32, device=dev),
+                "n_survivors": torch.empty(1, dtype=torch.int32, device=dev)}
+    _check(lib().tv_draft_reroot(
+        _ptr(parent), _ptr(token), _ptr(cum), n, _ptr(accepted["path"]), _ptr(accepted["m"]),
+        _ptr(accepted["out_tokens"]), prefix_len, _ptr(outs["new_pos"]), _ptr(outs["new_parent"]),
+        _ptr(outs["new_token"]), _ptr(outs["new_cum"]), _ptr(outs["n_survivors"]), _ptr(status),
+        _stream(stream, parent.device)), "tv_draft_reroot")
+    return outs

@@ -151,4 +151,51 @@ tv_status tv_kv_compact(void* k_cache, void* v_cache, int32_t n_layers,
                                       dev_status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static bool expand_args_ok(int32_t n_frontier, int32_t vocab, int32_t w) {
+  if (vocab < 1 || vocab > TV_MAX_VOCAB) return false;
+  if (n_frontier < 1 || n_frontier > TV_MAX_NODES) return false;
+  if (w < 1 || w > TV_MAX_EXPAND_WIDTH) return false;
+  if ((int64_t)n_frontier * w > TV_MAX_EXPAND_CANDIDATES) return false;
+  if ((int64_t)((vocab + 8191) / 8192) * w > TV_MAX_EXPAND_CANDIDATES) return false;
+  return (int64_t)w <= (int64_t)n_frontier * vocab;
+}
+
+size_t tv_expand_workspace_size(int32_t n_frontier, int32_t vocab, int32_t w) {
+  if (!expand_args_ok(n_frontier, vocab, w)) return 0;
+  return tv::plan_expand(n_frontier, vocab, w).ws_bytes;
+}
+
+tv_status tv_tree_expand(const float* logits, int32_t vocab, int32_t n_frontier,
+                         const int32_t* frontier, const float* cum, int32_t n_nodes, int32_t w,
+                         int32_t* new_parent, int32_t* new_token, float* new_score,
+                         void* workspace, size_t ws_bytes, int32_t* dev_status,
+                         tv_stream_t stream) {
+  if (!logits || !frontier || !cum || !new_parent || !new_token || !new_score || !workspace)
+    return TV_ERR_INVALID_ARG;
+  if (!expand_args_ok(n_frontier, vocab, w) || n_nodes < 1) return TV_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(logits) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(workspace) & 3u) != 0)
+    return TV_ERR_INVALID_ARG;
+  if (ws_bytes < tv::plan_expand(n_frontier, vocab, w).ws_bytes) return TV_ERR_CAPACITY;
+  return from_cuda(tv::launch_expand(logits, vocab, n_frontier, frontier, cum, n_nodes, w,
+                                     new_parent, new_token, new_score, workspace, dev_status,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tv_status tv_draft_reroot(const int32_t* parent, const int32_t* token, const float* cum,
+                          int32_t n_nodes, const int32_t* path, const int32_t* m,
+                          const int32_t* out_tokens, int32_t prefix_len, int32_t* new_pos,
+                          int32_t* new_parent, int32_t* new_token, float* new_cum,
+                          int32_t* n_survivors, int32_t* dev_status, tv_stream_t stream) {
+  if (!parent || !token || !cum || !path || !m || !out_tokens || !new_pos || !new_parent ||
+      !new_token || !new_cum || !n_survivors)
+    return TV_ERR_INVALID_ARG;
+  if (n_nodes < 1 || n_nodes > TV_MAX_NODES || prefix_len < 0) return TV_ERR_INVALID_ARG;
+  if ((int64_t)prefix_len + n_nodes > INT32_MAX) return TV_ERR_INVALID_ARG;
+  return from_cuda(tv::launch_draft_reroot(parent, token, cum, n_nodes, path, m, out_tokens,
+                                           prefix_len, new_pos, new_parent, new_token, new_cum,
+                                           n_survivors, dev_status,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -67,6 +67,22 @@ cudaError_t launch_accept(const float* logits, int32_t vocab, const int32_t* tok
                           int32_t* new_parent, int32_t* n_survivors, int32_t* dev_status,
                           cudaStream_t s);
 
+// Maximum-likelihood expansion: slices of each frontier logits row.
+struct ExpandPlan {
+  int chunks;      // slices per row
+  int chunk_len;   // logits per slice (a multiple of 4)
+  size_t ws_bytes; // workspace: one record per (row, slice)
+};
+ExpandPlan plan_expand(int32_t n_frontier, int32_t vocab, int32_t w);
+cudaError_t launch_expand(const float* logits, int32_t vocab, int32_t n_frontier,
+                          const int32_t* frontier, const float* cum, int32_t n_nodes, int32_t w,
+                          int32_t* new_parent, int32_t* new_token, float* new_score, void* ws,
+                          int32_t* dev_status, cudaStream_t s);
+cudaError_t launch_draft_reroot(const int32_t* parent, const int32_t* token, const float* cum,
+                                int32_t n, const int32_t* path, const int32_t* m,
+                                const int32_t* out_tokens, int32_t prefix, int32_t* new_pos,
+                                int32_t* new_parent, int32_t* new_token, float* new_cum,
+                                int32_t* n_survivors, int32_t* dev_status, cudaStream_t s);
 cudaError_t launch_compact(void* k, void* v, int32_t layers, int64_t layer_stride_bytes,
                            int32_t hkv, int64_t cap, int32_t row_bytes, int32_t prefix,
                            int32_t n, const int32_t* new_pos, int32_t* dev_status,

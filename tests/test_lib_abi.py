@@ -87,3 +87,34 @@ def test_workspace_size_is_monotone_in_prefix(lib):
         assert s >= last or s > 0
         last = s
     assert lib.tv_attn_workspace_size(64, 64, 8, 96, 1, 100) == 0
+
+
+def test_draft_side_host_checks(lib):
+    import ctypes
+    fake = ctypes.c_void_p(0x1000)
+    assert lib.tv_expand_workspace_size(8, 128256, 8) > 0
+    assert lib.tv_expand_workspace_size(0, 100, 8) == 0
+    assert lib.tv_expand_workspace_size(8, 100, 65) == 0           # w above the limit
+    assert lib.tv_expand_workspace_size(64, 100, 32) == 0          # n_frontier * w too large
+    assert lib.tv_expand_workspace_size(1, 4, 5) == 0              # w above n_frontier * vocab
+    assert lib.tv_expand_workspace_size(1, 600000, 8) == 0         # vocab above the limit
+    assert lib.tv_expand_workspace_size(1, 131072, 64) > 0
+    assert lib.tv_expand_workspace_size(1, 131073, 64) == 0        # ceil(V / 8192) * w
+
+    def expand(**kw):
+        a = dict(lg=fake, V=1000, F=4, fr=fake, cum=fake, N=10, w=8, ws=fake, wsb=1 << 30)
+        a.update(kw)
+        return lib.tv_tree_expand(a["lg"], a["V"], a["F"], a["fr"], a["cum"], a["N"], a["w"],
+                                  fake, fake, fake, a["ws"], a["wsb"], None, None)
+    assert expand(lg=None) == 1
+    assert expand(w=0) == 1
+    assert expand(F=200) == 1
+    assert expand(N=0) == 1
+    assert expand(lg=ctypes.c_void_p(0x1002)) == 1                 # misaligned logits
+    assert expand(wsb=16) == 3                                     # workspace too small
+    assert lib.tv_draft_reroot(None, fake, fake, 5, fake, fake, fake, 0, fake, fake, fake,
+                               fake, fake, None, None) == 1
+    assert lib.tv_draft_reroot(fake, fake, fake, 0, fake, fake, fake, 0, fake, fake, fake,
+                               fake, fake, None, None) == 1
+    assert lib.tv_draft_reroot(fake, fake, fake, 129, fake, fake, fake, 0, fake, fake, fake,
+                               fake, fake, None, None) == 1
