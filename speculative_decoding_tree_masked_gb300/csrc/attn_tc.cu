@@ -28,6 +28,12 @@
 // order, so S_t(j+1) being complete implies PV_t(j) is complete: the softmax
 // may then rescale O_t in place before releasing P_t(j+1).
 //
+// A CTA with a single row tile (G * N <= 128 rows per KV head) uses the
+// second tile's score columns as a second score buffer instead: QK^T(j + 2)
+// is issued right after PV(j), so the tensor core computes the next block's
+// scores while the softmax works on the current one, and a rescale of O
+// waits for the previous PV on its own barrier.
+//
 // Online softmax with a lazily moved maximum: the running maximum m used for
 // exponentiation is only raised when a block's maximum exceeds it by more
 // than 2^8 in probability, which bounds every P value by 256 and keeps the
@@ -93,7 +99,7 @@ struct Layout {
   static constexpr uint32_t kV = kK + kStages * kKV;
   static constexpr uint32_t kPar = kV + kStages * kKV;
   static constexpr uint32_t kBar = kPar + kMaxNodes * 4;
-  static constexpr uint32_t kNumBars = 3 * kTiles + 4 * kStages + kTiles + 1;
+  static constexpr uint32_t kNumBars = 3 * kTiles + 4 * kStages + kTiles + 2;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kMisc + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // slack to align the base to 1024
@@ -113,6 +119,8 @@ struct Bars {
   __device__ uint32_t epi(int t) const { return base + 8 * (3 * kTiles + 4 * kStages + t); }
   // the Q tiles have landed (TMA path)
   __device__ uint32_t q_full() const { return base + 8 * (4 * kTiles + 4 * kStages); }
+  // a PV product has completed (one tile with double-buffered scores)
+  __device__ uint32_t o_done() const { return base + 8 * (4 * kTiles + 4 * kStages + 1); }
 };
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -188,6 +196,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   const int kbeg = split * p.keys_per_split;
   const int kend = min(p.keys, kbeg + p.keys_per_split);
   const int nb = (kend - kbeg + kBN - 1) / kBN;
+  // With a single row tile the second tile's score columns are free: the
+  // scores are double-buffered, so that QK^T of block j + 1 runs while the
+  // softmax works on block j.
+  const bool db = ntiles == 1;
 
   const Bars bars{base + L::kBar};
   int32_t* par = reinterpret_cast<int32_t*>(sm + L::kPar);
@@ -210,6 +222,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       ptx::mbar_init(bars.epi(t), kWarpsPerTile);
     }
     ptx::mbar_init(bars.q_full(), 1);
+    ptx::mbar_init(bars.o_done(), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -300,8 +313,29 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       // slot is refilled as soon as the last QK^T reading it is done and a V
       // slot once the last PV reading it is done: keys run about half a
       // block ahead of values.
-      if (nb > 0 && wait_bar(bars.k_full(0), 0, abort_flag, p.dev_status)) load_v(0);
-      for (int j = 1; j < nb; ++j) {
+      if (db) {
+        // double-buffered scores: QK^T runs a block ahead of PV, so keys are
+        // requested a block ahead of values (K_0, K_1, V_0, K_2, V_1, ...)
+        bool ok = nb > 0 && wait_bar(bars.k_full(0), 0, abort_flag, p.dev_status);
+        if (ok && nb > 1) load_k(1);
+        if (ok) load_v(0);
+        for (int j = 1; ok && j < nb; ++j) {
+          if (j + 1 < nb) {
+            const int s = (j + 1) % kStages, u = (j + 1) / kStages;
+            if (j + 1 >= kStages)
+              ok = wait_bar(bars.k_empty(s), (u - 1) & 1, abort_flag, p.dev_status);
+            if (!ok) break;
+            load_k(j + 1);
+          }
+          const int s = j % kStages, u = j / kStages;
+          if (j >= kStages) ok = wait_bar(bars.v_empty(s), (u - 1) & 1, abort_flag, p.dev_status);
+          if (!ok) break;
+          load_v(j);
+        }
+      } else if (nb > 0 && wait_bar(bars.k_full(0), 0, abort_flag, p.dev_status)) {
+        load_v(0);
+      }
+      for (int j = 1; !db && j < nb; ++j) {
         const int s = j % kStages, u = j / kStages;
         bool ready = j < kStages ? true
                                  : wait_bar(bars.k_empty(s), (u - 1) & 1, abort_flag, p.dev_status);
@@ -326,25 +360,71 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       // V block, MN-major: 8-key groups 1024 B apart (SBO), the two 64-column
       // halves of d kBN * 128 B apart (LBO)
       const uint64_t v_desc = ptx::smem_desc_sw128(base + L::kV, kBN * 128, 1024);
-      auto issue_qk = [&](int t, int s) {
+      // S buffer b (TMEM columns [128 b, 128 b + 128)) = Q tile t . K slot s
+      auto issue_qk_to = [&](int t, int b, int s) {
         const uint64_t qd = q_desc + ((t * L::kQTile) >> 4);
         const uint64_t kd = k_desc + ((s * L::kKV) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t qo = ((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4;
           const uint32_t ko = ((kk >> 2) * (kBN * 128) + (kk & 3) * 32) >> 4;
-          ptx::mma_ss(tmem + t * kBN, qd + qo, kd + ko, kIdescQK, kk > 0 ? 1u : 0u);
+          ptx::mma_ss(tmem + b * kBN, qd + qo, kd + ko, kIdescQK, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int t, int s, bool acc) {
+      // O_t (+)= P in S buffer b . V slot s
+      auto issue_pv_from = [&](int b, int t, int s, bool acc) {
         const uint64_t vd = v_desc + ((s * L::kKV) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          ptx::mma_ts(tmem + 2 * kBN + t * D, tmem + t * kBN + kk * 8, vd + ((kk * 2048) >> 4),
+          ptx::mma_ts(tmem + 2 * kBN + t * D, tmem + b * kBN + kk * 8, vd + ((kk * 2048) >> 4),
                       kIdescPV, (acc || kk > 0) ? 1u : 0u);
       };
+      auto issue_qk = [&](int t, int s) { issue_qk_to(t, t, s); };
+      auto issue_pv = [&](int t, int s, bool acc) { issue_pv_from(t, t, s, acc); };
       bool ok = nb > 0 && wait_bar(bars.k_full(0), 0, abort_flag, p.dev_status);
       if (ok && p.q_tma) ok = wait_bar(bars.q_full(), 0, abort_flag, p.dev_status);
+      if (db) {
+        // one tile, scores in two buffers: QK^T(j + 2) is issued right after
+        // PV(j) has freed buffer j % 2; MMAs from one thread run in order, so
+        // PV(j) reads P before QK^T overwrites it
+        if (ok) {
+          ptx::tc_fence_after();
+          issue_qk_to(0, 0, 0);
+          ptx::mma_commit(bars.s_full(0));
+          ptx::mma_commit(bars.k_empty(0));
+        }
+        if (ok && nb > 1) {
+          ok = wait_bar(bars.k_full(1), 0, abort_flag, p.dev_status);
+          if (ok) {
+            ptx::tc_fence_after();
+            issue_qk_to(0, 1, 1);
+            ptx::mma_commit(bars.s_full(1));
+            ptx::mma_commit(bars.k_empty(1));
+          }
+        }
+        for (int j = 0; ok && j < nb; ++j) {
+          const int b = j & 1;
+          const int s = j % kStages, u = j / kStages;
+          ok = wait_bar(bars.v_full(s), u & 1, abort_flag, p.dev_status);
+          if (ok) ok = wait_bar(bars.p_full(b), (j >> 1) & 1, abort_flag, p.dev_status);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_pv_from(b, 0, s, j > 0);
+          ptx::mma_commit(bars.o_done());
+          ptx::mma_commit(bars.v_empty(s));
+          if (j + 2 < nb) {
+            const int s2 = (j + 2) % kStages, u2 = (j + 2) / kStages;
+            ok = wait_bar(bars.k_full(s2), u2 & 1, abort_flag, p.dev_status);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            issue_qk_to(0, b, s2);
+            ptx::mma_commit(bars.s_full(b));
+            ptx::mma_commit(bars.k_empty(s2));
+          }
+          if (j + 1 == nb) ptx::mma_commit(bars.o_final(0));
+        }
+        ok = false;  // the two-tile loop below is not for this CTA
+      }
       if (ok) {
         ptx::tc_fence_after();
         for (int t = 0; t < ntiles; ++t) {
@@ -405,14 +485,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       for (int w = 0; w < kMaskWords; ++w) anc[w] = 0u;
       if (row_ok && !ancestor_bits(par, grow / G, anc)) report(p.dev_status, TV_ERR_INVALID_TREE);
       const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-      const uint32_t t_s = tmem + lane_base + t * kBN;
       const uint32_t t_o = tmem + lane_base + 2 * kBN + t * D;
       const float c = p.scale_log2;
       const float rescale_raw = kRescaleLog2 / c;
       float m_used = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < nb; ++j) {
-        ok = wait_bar(bars.s_full(t), j & 1, abort_flag, p.dev_status);
+        // the score buffer of this block and the phase of its barriers
+        const int b = db ? (j & 1) : t;
+        const uint32_t ph = db ? ((j >> 1) & 1) : (j & 1);
+        const uint32_t t_s = tmem + lane_base + b * kBN;
+        ok = wait_bar(bars.s_full(b), ph, abort_flag, p.dev_status);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         ptx::tc_fence_after();
         const int kb0 = kbeg + j * kBN;
@@ -483,8 +566,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         }
         l = l * alpha + (sum0 + sum1);
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
-          // O_t holds the sum through block j-1 (complete, see above) and
-          // PV_t(j) waits for this thread's P_full arrival
+          // O_t must hold the sum through block j-1.  With one buffer per
+          // tile, S_t(j) complete implies PV_t(j-1) complete (see above);
+          // with double-buffered scores PV(j-1) may still run: wait for it.
+          // PV_t(j) waits for this thread's P_full arrival.
+          if (db && !wait_bar(bars.o_done(), (j - 1) & 1, abort_flag, p.dev_status)) ok = false;
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          ptx::tc_fence_after();
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
             uint32_t v[32];
@@ -498,7 +586,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bars.p_full(t));
+        if (lane == 0) ptx::mbar_arrive(bars.p_full(b));
       }
       // epilogue: O_t is final once the last PV has completed
       if (ok) ok = wait_bar(bars.o_final(t), 0, abort_flag, p.dev_status);

@@ -191,3 +191,20 @@ def test_tree_mask_words_match_oracle(n):
     parent = synth.random_parent_tree(rng, n, max_depth=16)
     words = tvp.tree_mask(torch.from_numpy(parent).to(DEV)).cpu().numpy().view(np.uint32)
     assert np.array_equal(words, oracle.ancestor_bitmask(parent))
+
+
+@pytest.mark.parametrize("grow", [0.0, 3.0])
+def test_single_tile_with_late_maxima(grow):
+    # G * N <= 128 rows per KV head: one row tile per CTA, whose scores are
+    # double-buffered.  Key norms growing along the prefix make later blocks
+    # raise the running maximum, which rescales O while the previous PV may
+    # still be in flight.
+    rng = np.random.default_rng(7)
+    n, P, hq, hkv, d = 8, 8192, 64, 8, 128
+    parent = synth.random_parent_tree(rng, n, max_depth=4)
+    q, k, v = _qkv(rng, n, hq, hkv, d, P + n, torch.bfloat16)
+    ramp = torch.from_numpy((1.0 + grow * np.arange(P + n) / (P + n)).astype(np.float32))
+    k = (k.float() * ramp[None, :, None]).to(torch.bfloat16)
+    out = _run(q, k, v, P, parent)
+    nodes = [0, 3, 7]
+    assert _err(out, _ref(q, k, v, P, parent, nodes=nodes), nodes) <= BF16_TOL
