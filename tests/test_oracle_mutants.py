@@ -226,3 +226,38 @@ def test_unrebased_path_scores_are_caught(monkeypatch):
         return res
     monkeypatch.setattr(exp.oracle, "draft_reroot", no_rebase)
     assert _some_fail(_reroot_pins())
+
+
+# ------------------------------------------------------------ sampling
+
+import oracle.tree_sample as ts  # noqa: E402
+from tests import test_oracle_sample as smp  # noqa: E402
+
+
+def _sample_pins():
+    return [lambda: smp.check_drawn_distribution(0.5), lambda: smp.check_drawn_distribution(2.0),
+            smp.test_inversion_edges, lambda: smp.test_philox_matches_numpy((1, 2))]
+
+
+def test_sampling_pins_pass_unmutated():
+    assert not _some_fail(_sample_pins())
+
+
+def test_temperature_multiplied_is_caught(monkeypatch):
+    orig = ts.target_probs
+    monkeypatch.setattr(ts, "target_probs", lambda logits, T: orig(logits, 1.0 / T))
+    assert _some_fail(_sample_pins())
+
+
+def test_inversion_at_or_above_is_caught(monkeypatch):
+    def left(probs_row, u):
+        c = np.cumsum(np.asarray(probs_row, dtype=np.float64))
+        return int(min(np.searchsorted(c, u, side="left"), len(c) - 1))
+    monkeypatch.setattr(ts, "draw_by_inversion", left)
+    monkeypatch.setattr(smp.oracle, "draw_by_inversion", left)
+    assert _some_fail(_sample_pins())
+
+
+def test_philox_without_key_schedule_is_caught(monkeypatch):
+    monkeypatch.setattr(ts, "_W0", 0)
+    assert _some_fail(_sample_pins())
