@@ -610,6 +610,64 @@ def run_expand(args, local_rank):
         "peak_source": peaks["source"]}), flush=True)
 
 
+def run_sample(args, local_rank):
+    """Acceptance alone at the full step's shape (64 tree nodes, vocabulary
+    128256, float32 logits, 32.8 MB): greedy (argmax) and sampling at T = 1,
+    each over enough logits copies to exceed L2.  One JSON line."""
+    import numpy as np
+    import torch
+
+    import speculative_decoding_tree_masked_gb300 as tvp
+    from workloads import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.Stream(dev)
+    peaks = _peaks()
+    w = synth.make_workload(WORKLOAD, seed=args.seed, layers=1)
+    base = torch.from_numpy(w.logits).to(dev)
+    copies = max(3, -(-3 * 130_000_000 // base.numel() // 4))
+    logits = [base] + [base.clone() for _ in range(copies - 1)]
+    token = torch.from_numpy(w.token).to(dev)
+    parent = torch.from_numpy(w.parent).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    outs_g = tvp.tree_accept(base, token, parent, PREFIX, status=status)
+    outs_s = tvp.tree_accept_sampled(base, token, parent, PREFIX, 1.0, args.seed, 0,
+                                     status=status)
+    res = {}
+    for name, call in (
+            ("greedy", lambda c: tvp.tree_accept(logits[c], token, parent, PREFIX, outs=outs_g,
+                                                 status=status)),
+            ("sampled", lambda c: tvp.tree_accept_sampled(logits[c], token, parent, PREFIX, 1.0,
+                                                          args.seed, c, outs=outs_s,
+                                                          status=status))):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for c in range(copies):
+                call(c)
+        reps = max(3, args.steps)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                graph.replay()
+            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ea.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            eb.record(stream)
+        torch.cuda.synchronize()
+        res[name] = ea.elapsed_time(eb) * 1e3 / (reps * copies)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in acceptance")
+    nbytes = base.numel() * 4
+    print(json.dumps({
+        "kernel": "tree acceptance (target token per node + walk + re-root map)",
+        "workload": f"{NODES} tree nodes x vocab {VOCAB} (float32 logits)",
+        "us_per_call": res, "bytes": nbytes,
+        "hbm_frac": {k: nbytes / v / 1e3 / peaks["hbm_gbs"] for k, v in res.items()},
+        "l2": f"{copies} copies of the logits cycled (larger than L2)",
+        "peak_source": peaks["source"]}), flush=True)
+
+
 def _splits_for(tvp, n, hq, hkv, d, prefix):
     import torch
     nbytes = tvp.attn_workspace_size(n, hq, hkv, d, torch.bfloat16, prefix)
@@ -636,6 +694,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layers of KV per step (a smaller case for profiling)")
+    ap.add_argument("--sample", action="store_true",
+                    help="time greedy and sampling acceptance instead of the step")
     ap.add_argument("--expand", action="store_true",
                     help="time the draft side's tree expansion instead of the step")
     ap.add_argument("--sweep", action="store_true",
@@ -650,9 +710,10 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
-    if args.sweep or args.expand:
+    if args.sweep or args.expand or args.sample:
         if rank == 0:
-            (run_sweep if args.sweep else run_expand)(args, local_rank)
+            (run_sweep if args.sweep else run_expand if args.expand else run_sample)(
+                args, local_rank)
         return
     if world > 1:
         import torch

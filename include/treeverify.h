@@ -234,6 +234,39 @@ TV_API tv_status tv_tree_accept(const float* logits, int32_t vocab, const int32_
                          int32_t* dev_status, tv_stream_t stream);
 
 /*
+ * tv_tree_accept_sampled -- sampling (stochastic) verification of the draft
+ * tree at temperature T, with the outputs of tv_tree_accept.
+ *
+ * The SwiftSpec review page verifies greedily ("What carries the argument":
+ * the verified tokens are the target's) and is silent on sampling; this is
+ * the library's reading for trees grown deterministically by
+ * maximum-likelihood expansion ("Assumptions & free parameters").  At every
+ * node i the target's token is drawn from p_i = softmax(logits[i] / T) by
+ * inversion: the smallest v with p_i[0] + ... + p_i[v] > u_i, where u_i is
+ * the uniform (x0 >> 11 + 1/2) / 2^53 from the first word x0 of
+ * Philox4x64-10 (Salmon et al., SC 2011) with key (seed, 0) and counter
+ * (i, offset, 0, 0).  The walk is tv_tree_accept's with the drawn tokens in
+ * place of the argmax, so every emitted token is the target's own draw at its
+ * context (the step is lossless).  The draws are made in float32 with double
+ * sums: a u within about 1e-6 of a cumulative-probability boundary may fall
+ * on either side of it.
+ *
+ *   temperature  T > 0 and finite (0 is the greedy tv_tree_accept)
+ *   seed, offset the generator's key and the counter's second word; use a
+ *                new offset for every verification step
+ *   sampled      device int32 [n_nodes], written: the drawn token per node
+ *                (-1 for a node whose logits are all -inf)
+ * Other arguments and outputs: as tv_tree_accept (logits finite or -inf).
+ */
+TV_API tv_status tv_tree_accept_sampled(const float* logits, int32_t vocab, const int32_t* token,
+                                        const int32_t* parent, int32_t n_nodes,
+                                        int32_t prefix_len, float temperature, uint64_t seed,
+                                        uint64_t offset, int32_t* sampled, int32_t* m,
+                                        int32_t* path, int32_t* out_tokens, int32_t* new_pos,
+                                        int32_t* new_parent, int32_t* n_survivors,
+                                        int32_t* dev_status, tv_stream_t stream);
+
+/*
  * tv_kv_compact -- in-place reorganisation of the K and V caches of every
  * layer after a verification.
  *

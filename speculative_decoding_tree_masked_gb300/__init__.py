@@ -172,6 +172,34 @@ def tree_accept(logits: torch.Tensor, token: torch.Tensor, parent: torch.Tensor,
     return outs
 
 
+def tree_accept_sampled(logits: torch.Tensor, token: torch.Tensor, parent: torch.Tensor,
+                        prefix_len: int, temperature: float, seed: int, offset: int,
+                        outs: Optional[dict] = None, status: Optional[torch.Tensor] = None,
+                        stream=None) -> dict:
+    """Sampling verification at temperature T: the target's token at every
+    node drawn from softmax(logits / T) with a counter-based generator keyed
+    by (seed, offset), then the walk of tree_accept over the drawn tokens.
+    Returns the dict of tree_accept with "sampled" [N] in place of "am"."""
+    _need_cuda(logits, token, parent)
+    n, vocab = logits.shape
+    if logits.dtype != torch.float32 or token.dtype != torch.int32 or parent.dtype != torch.int32:
+        raise ValueError("dtype mismatch")
+    if token.numel() != n or parent.numel() != n:
+        raise ValueError("shape mismatch")
+    if outs is None:
+        dev = logits.device
+        outs = {k: torch.empty(sz, dtype=torch.int32, device=dev) for k, sz in (
+            ("sampled", n), ("m", 1), ("path", n), ("out_tokens", n + 1), ("new_pos", n),
+            ("new_parent", n), ("n_survivors", 1))}
+    _check(lib().tv_tree_accept_sampled(
+        _ptr(logits), vocab, _ptr(token), _ptr(parent), n, prefix_len, float(temperature),
+        int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), _ptr(outs["sampled"]),
+        _ptr(outs["m"]), _ptr(outs["path"]), _ptr(outs["out_tokens"]), _ptr(outs["new_pos"]),
+        _ptr(outs["new_parent"]), _ptr(outs["n_survivors"]), _ptr(status),
+        _stream(stream, logits.device)), "tv_tree_accept_sampled")
+    return outs
+
+
 def kv_compact(k_cache: torch.Tensor, v_cache: torch.Tensor, prefix_len: int, n_nodes: int,
                new_pos: torch.Tensor, status: Optional[torch.Tensor] = None,
                stream=None) -> None:

@@ -52,14 +52,26 @@ argmax_kernel(const float* __restrict__ logits, int vocab, int32_t* __restrict__
   int bi = INT_MAX;
   const bool vec = ((vocab & 3) == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
   if (vec) {
+    // four float4 loads per thread in flight before any is compared
     const float4* b4 = reinterpret_cast<const float4*>(base);
-    for (int i4 = beg / 4 + tid; i4 < end / 4; i4 += kArgmaxThreads) {
-      const float4 x = __ldcs(b4 + i4);
-      const int i = i4 * 4;
-      if (better(x.x, i, bv, bi)) { bv = x.x; bi = i; }
-      if (better(x.y, i + 1, bv, bi)) { bv = x.y; bi = i + 1; }
-      if (better(x.z, i + 2, bv, bi)) { bv = x.z; bi = i + 2; }
-      if (better(x.w, i + 3, bv, bi)) { bv = x.w; bi = i + 3; }
+    const int e4 = end / 4;
+    for (int i40 = beg / 4 + tid; i40 < e4; i40 += 4 * kArgmaxThreads) {
+      float4 x[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i4 = i40 + q * kArgmaxThreads;
+        x[q] = i4 < e4 ? __ldcs(b4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i4 = i40 + q * kArgmaxThreads;
+        if (i4 >= e4) break;
+        const int i = i4 * 4;
+        if (better(x[q].x, i, bv, bi)) { bv = x[q].x; bi = i; }
+        if (better(x[q].y, i + 1, bv, bi)) { bv = x[q].y; bi = i + 1; }
+        if (better(x[q].z, i + 2, bv, bi)) { bv = x[q].z; bi = i + 2; }
+        if (better(x[q].w, i + 3, bv, bi)) { bv = x[q].w; bi = i + 3; }
+      }
     }
   } else {
     for (int i = beg + tid; i < end; i += kArgmaxThreads) {
@@ -213,6 +225,14 @@ cudaError_t launch_accept(const float* logits, int32_t vocab, const int32_t* tok
   argmax_kernel<<<dim3(kArgmaxCluster, n), kArgmaxThreads, 0, s>>>(logits, vocab, am);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  return launch_walk(token, parent, am, n, vocab, prefix, m, path, out_tokens, new_pos,
+                     new_parent, n_survivors, dev_status, s);
+}
+
+cudaError_t launch_walk(const int32_t* token, const int32_t* parent, const int32_t* am,
+                        int32_t n, int32_t vocab, int32_t prefix, int32_t* m, int32_t* path,
+                        int32_t* out_tokens, int32_t* new_pos, int32_t* new_parent,
+                        int32_t* n_survivors, int32_t* dev_status, cudaStream_t s) {
   walk_kernel<<<1, 32, 0, s>>>(token, parent, am, n, vocab, prefix, m, path, out_tokens,
                                new_pos, new_parent, n_survivors, dev_status);
   return cudaGetLastError();

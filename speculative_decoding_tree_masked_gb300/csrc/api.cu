@@ -132,6 +132,26 @@ tv_status tv_tree_accept(const float* logits, int32_t vocab, const int32_t* toke
                                      dev_status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+tv_status tv_tree_accept_sampled(const float* logits, int32_t vocab, const int32_t* token,
+                                 const int32_t* parent, int32_t n_nodes, int32_t prefix_len,
+                                 float temperature, uint64_t seed, uint64_t offset,
+                                 int32_t* sampled, int32_t* m, int32_t* path, int32_t* out_tokens,
+                                 int32_t* new_pos, int32_t* new_parent, int32_t* n_survivors,
+                                 int32_t* dev_status, tv_stream_t stream) {
+  if (!logits || !token || !parent || !sampled || !m || !path || !out_tokens || !new_pos ||
+      !new_parent || !n_survivors)
+    return TV_ERR_INVALID_ARG;
+  if (vocab < 1 || n_nodes < 1 || n_nodes > TV_MAX_NODES || prefix_len < 0)
+    return TV_ERR_INVALID_ARG;
+  if (!(temperature > 0.f) || std::isinf(temperature)) return TV_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(logits) & 3u) != 0) return TV_ERR_INVALID_ARG;
+  if ((int64_t)prefix_len + n_nodes > INT32_MAX) return TV_ERR_INVALID_ARG;
+  return from_cuda(tv::launch_accept_sampled(logits, vocab, token, parent, n_nodes, prefix_len,
+                                             temperature, seed, offset, sampled, m, path,
+                                             out_tokens, new_pos, new_parent, n_survivors,
+                                             dev_status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 tv_status tv_kv_compact(void* k_cache, void* v_cache, int32_t n_layers,
                         int64_t layer_stride_elems, int32_t hkv, int64_t cap, int32_t d,
                         int32_t dtype, int32_t prefix_len, int32_t n_nodes,

@@ -83,6 +83,18 @@ cudaError_t launch_draft_reroot(const int32_t* parent, const int32_t* token, con
                                 const int32_t* out_tokens, int32_t prefix, int32_t* new_pos,
                                 int32_t* new_parent, int32_t* new_token, float* new_cum,
                                 int32_t* n_survivors, int32_t* dev_status, cudaStream_t s);
+// The greedy walk and re-root map from per-node target tokens am (the
+// argmax, or the sampled tokens).
+cudaError_t launch_walk(const int32_t* token, const int32_t* parent, const int32_t* am,
+                        int32_t n, int32_t vocab, int32_t prefix, int32_t* m, int32_t* path,
+                        int32_t* out_tokens, int32_t* new_pos, int32_t* new_parent,
+                        int32_t* n_survivors, int32_t* dev_status, cudaStream_t s);
+cudaError_t launch_accept_sampled(const float* logits, int32_t vocab, const int32_t* token,
+                                  const int32_t* parent, int32_t n, int32_t prefix,
+                                  float temperature, uint64_t seed, uint64_t offset,
+                                  int32_t* sampled, int32_t* m, int32_t* path,
+                                  int32_t* out_tokens, int32_t* new_pos, int32_t* new_parent,
+                                  int32_t* n_survivors, int32_t* dev_status, cudaStream_t s);
 cudaError_t launch_compact(void* k, void* v, int32_t layers, int64_t layer_stride_bytes,
                            int32_t hkv, int64_t cap, int32_t row_bytes, int32_t prefix,
                            int32_t n, const int32_t* new_pos, int32_t* dev_status,

@@ -118,3 +118,21 @@ def test_draft_side_host_checks(lib):
                                fake, fake, None, None) == 1
     assert lib.tv_draft_reroot(fake, fake, fake, 129, fake, fake, fake, 0, fake, fake, fake,
                                fake, fake, None, None) == 1
+
+
+def test_sampled_accept_host_checks(lib):
+    import ctypes
+    fake = ctypes.c_void_p(0x1000)
+
+    def call(**kw):
+        a = dict(lg=fake, V=100, n=4, T=1.0)
+        a.update(kw)
+        return lib.tv_tree_accept_sampled(a["lg"], a["V"], fake, fake, a["n"], 0, a["T"], 1, 0,
+                                          fake, fake, fake, fake, fake, fake, fake, None, None)
+    assert call(lg=None) == 1
+    assert call(T=0.0) == 1
+    assert call(T=-1.0) == 1
+    assert call(T=float("inf")) == 1
+    assert call(T=float("nan")) == 1
+    assert call(n=0) == 1
+    assert call(V=0) == 1
