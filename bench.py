@@ -668,6 +668,88 @@ def run_sample(args, local_rank):
         "peak_source": peaks["source"]}), flush=True)
 
 
+def run_batch(args, local_rank):
+    """Batched tree attention: 8 requests at 70B-class shapes (64/8 heads,
+    d128, bf16, 64-node trees) with ragged prefixes 1K, 2K, ..., 8K, one
+    layer each, as one batched call and as 8 single calls; every layer has
+    its own caches and three layers are cycled (larger than L2).  One JSON
+    line."""
+    import numpy as np
+    import torch
+
+    import speculative_decoding_tree_masked_gb300 as tvp
+    from workloads import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.Stream(dev)
+    peaks = _peaks()
+    prefixes = [1024 * (b + 1) for b in range(8)]
+    layers = 3
+    reqs = []
+    flops = 0
+    nbytes = 0
+    for b, P in enumerate(prefixes):
+        w = synth.make_workload("q2_72b", seed=args.seed + b, prefix=P, n=NODES)
+        q, k, v = synth.make_qkv(w, layer=0)
+        q, k, v = q.to(dev), k.to(dev), v.to(dev)
+        par = torch.from_numpy(w.parent).to(dev)
+        reqs.append((q, [k] + [k.clone() for _ in range(layers - 1)],
+                     [v] + [v.clone() for _ in range(layers - 1)], P, par))
+        nb, fl = _algorithmic_work(w.parent, P, NODES, HQ, HKV, D)
+        flops += fl
+        nbytes += nb
+    outs = [torch.empty_like(r[0]) for r in reqs]
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_b = torch.zeros(tvp.attn_batched_workspace_size([NODES] * 8, HQ, HKV, D, torch.bfloat16),
+                       dtype=torch.uint8, device=dev)
+    ws_s = [tvp.attn_workspace(NODES, HQ, HKV, D, torch.bfloat16, P, dev) for P in prefixes]
+
+    def batched():
+        for l in range(layers):
+            tvp.tree_attn_verify_batched([r[0] for r in reqs], [r[1][l] for r in reqs],
+                                         [r[2][l] for r in reqs], prefixes,
+                                         [r[4] for r in reqs], outs=outs, workspace=ws_b,
+                                         status=status)
+
+    def singles():
+        for l in range(layers):
+            for b, r in enumerate(reqs):
+                tvp.tree_attn_verify(r[0], r[1][l], r[2][l], r[3], r[4], out=outs[b],
+                                     workspace=ws_s[b], status=status)
+
+    res = {}
+    for name, fn in (("batched", batched), ("single_calls", singles)):
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            fn()
+        reps = max(3, args.steps)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                graph.replay()
+            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ea.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            eb.record(stream)
+        torch.cuda.synchronize()
+        res[name] = ea.elapsed_time(eb) * 1e3 / (reps * layers)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the batch")
+    print(json.dumps({
+        "kernel": "batched tree attention (one launch for 8 requests)",
+        "workload": "8 requests, 64/8 heads, d128, bf16, 64-node trees, prefixes 1K..8K",
+        "us_per_layer": res,
+        "tree_tokens_per_s_per_layer": {k: 8 * NODES / (v * 1e-6) for k, v in res.items()},
+        "tflops": {k: flops / v / 1e6 for k, v in res.items()},
+        "tensor_frac": {k: flops / v / 1e6 / peaks["bf16_tflops"] for k, v in res.items()},
+        "hbm_frac": {k: nbytes / v / 1e3 / peaks["hbm_gbs"] for k, v in res.items()},
+        "peak_source": peaks["source"]}), flush=True)
+
+
 def _splits_for(tvp, n, hq, hkv, d, prefix):
     import torch
     nbytes = tvp.attn_workspace_size(n, hq, hkv, d, torch.bfloat16, prefix)
@@ -694,6 +776,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layers of KV per step (a smaller case for profiling)")
+    ap.add_argument("--batch", action="store_true",
+                    help="time batched attention of 8 ragged requests instead of the step")
     ap.add_argument("--sample", action="store_true",
                     help="time greedy and sampling acceptance instead of the step")
     ap.add_argument("--expand", action="store_true",
@@ -710,10 +794,11 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
-    if args.sweep or args.expand or args.sample:
+    if args.sweep or args.expand or args.sample or args.batch:
         if rank == 0:
-            (run_sweep if args.sweep else run_expand if args.expand else run_sample)(
-                args, local_rank)
+            mode = (run_sweep if args.sweep else run_expand if args.expand else
+                    run_sample if args.sample else run_batch)
+            mode(args, local_rank)
         return
     if world > 1:
         import torch

@@ -189,6 +189,44 @@ TV_API tv_status tv_tree_attn_verify_static(const void* q, const void* k_cache,
                                             float scale, int32_t* dev_status, tv_stream_t stream);
 
 /*
+ * Batched tree attention: up to TV_MAX_BATCH requests (independent
+ * sequences, each with its own prefix length, tree and caches) in one launch
+ * of the tensor-core kernel.  The pages verify a single request; batching is
+ * the serving form of the same operation, and every request's output is
+ * exactly what tv_tree_attn_verify gives for it (up to rounding: the split
+ * plans differ).
+ */
+#define TV_MAX_BATCH 16
+
+/* Bytes of workspace tv_tree_attn_verify_batched needs for these node counts
+ * (any prefix lengths) on the current device; 0 for arguments it rejects
+ * (bf16 only). */
+TV_API size_t tv_attn_batched_workspace_size(int32_t batch, const int32_t* n_nodes, int32_t hq,
+                                             int32_t hkv, int32_t d, int32_t dtype);
+
+/*
+ * tv_tree_attn_verify_batched -- tv_tree_attn_verify for `batch` requests at
+ * once.  The per-request arguments are HOST arrays of `batch` entries:
+ *   q, k_cache, v_cache, out, parent   device pointers, as tv_tree_attn_verify
+ *   cap, prefix_len, n_nodes           sizes, as tv_tree_attn_verify
+ * hq, hkv, d, scale and dtype are shared; dtype must be TV_BF16 (other types
+ * return TV_ERR_UNSUPPORTED).  workspace: device memory of at least
+ * tv_attn_batched_workspace_size bytes, 16-byte aligned, contents on entry
+ * irrelevant.  Every check of tv_tree_attn_verify applies to every request
+ * and is made before anything is launched.  The key splits of the requests
+ * are sized in proportion to their key counts so that one launch keeps the
+ * GPU busy; requests with several splits are merged by one extra launch each.
+ */
+TV_API tv_status tv_tree_attn_verify_batched(int32_t batch, const void* const* q,
+                                             const void* const* k_cache,
+                                             const void* const* v_cache, const int64_t* cap,
+                                             const int32_t* prefix_len, const int32_t* n_nodes,
+                                             const int32_t* const* parent, void* const* out,
+                                             int32_t hq, int32_t hkv, int32_t d, int32_t dtype,
+                                             float scale, void* workspace, size_t ws_bytes,
+                                             int32_t* dev_status, tv_stream_t stream);
+
+/*
  * tv_tree_accept -- greedy acceptance of the draft tree and the re-root map.
  *
  * Passage: SwiftSpec review page, "What carries the argument" (the tree

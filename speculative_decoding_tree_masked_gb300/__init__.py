@@ -146,6 +146,55 @@ def tree_attn_verify_static(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
     return out
 
 
+def _host_array(ctype, values):
+    return (ctype * len(values))(*values)
+
+
+def attn_batched_workspace_size(n_nodes, hq: int, hkv: int, d: int, dtype: torch.dtype) -> int:
+    ns = _host_array(ctypes.c_int32, [int(x) for x in n_nodes])
+    return int(lib().tv_attn_batched_workspace_size(len(ns), ctypes.cast(ns, ctypes.c_void_p),
+                                                    hq, hkv, d, _DTYPES[dtype]))
+
+
+def tree_attn_verify_batched(qs, k_caches, v_caches, prefix_lens, parents, outs=None,
+                             scale: float = 0.0, workspace: Optional[torch.Tensor] = None,
+                             status: Optional[torch.Tensor] = None, stream=None) -> list:
+    """Tree attention for several requests in one launch (bf16).  Lists of
+    per-request tensors: q [N_b][Hq][d], caches [Hkv][cap_b][d], parent int32
+    [N_b]; prefix_lens a list of ints.  Returns the list of outputs."""
+    batch = len(qs)
+    if not (len(k_caches) == len(v_caches) == len(prefix_lens) == len(parents) == batch):
+        raise ValueError("per-request lists differ in length")
+    _need_cuda(*qs, *k_caches, *v_caches, *parents)
+    hq, d = qs[0].shape[1], qs[0].shape[2]
+    hkv = k_caches[0].shape[0]
+    for q, k, v, par in zip(qs, k_caches, v_caches, parents):
+        if q.shape[1:] != (hq, d) or k.shape[0] != hkv or k.shape[2] != d or \
+                v.shape != k.shape or par.numel() != q.shape[0]:
+            raise ValueError("shape mismatch")
+        if q.dtype != qs[0].dtype or k.dtype != q.dtype or v.dtype != q.dtype or \
+                par.dtype != torch.int32:
+            raise ValueError("dtype mismatch")
+    if outs is None:
+        outs = [torch.empty_like(q) for q in qs]
+    ns = [q.shape[0] for q in qs]
+    if workspace is None:
+        nbytes = attn_batched_workspace_size(ns, hq, hkv, d, qs[0].dtype)
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=qs[0].device)
+    vp = lambda ts: _host_array(ctypes.c_void_p, [_ptr(t) for t in ts])
+    arrs = [vp(qs), vp(k_caches), vp(v_caches),
+            _host_array(ctypes.c_int64, [k.shape[1] for k in k_caches]),
+            _host_array(ctypes.c_int32, [int(x) for x in prefix_lens]),
+            _host_array(ctypes.c_int32, ns), vp(parents), vp(outs)]
+    cp = [ctypes.cast(a, ctypes.c_void_p) for a in arrs]
+    _check(lib().tv_tree_attn_verify_batched(
+        batch, cp[0], cp[1], cp[2], cp[3], cp[4], cp[5], cp[6], cp[7], hq, hkv, d,
+        _dtype_code(qs[0]), float(scale), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(status),
+        _stream(stream, qs[0].device)), "tv_tree_attn_verify_batched")
+    return outs
+
+
 def tree_accept(logits: torch.Tensor, token: torch.Tensor, parent: torch.Tensor, prefix_len: int,
                 outs: Optional[dict] = None, status: Optional[torch.Tensor] = None,
                 stream=None) -> dict:

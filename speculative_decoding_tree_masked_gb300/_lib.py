@@ -29,6 +29,10 @@ SIGNATURES = {
     "tv_tree_attn_verify_static": (c_i32, [c_ptr, c_ptr, c_ptr, c_i64, c_i32, c_i32, c_ptr,
                                            c_ptr, c_i32, c_i32, c_i32, c_i32, ctypes.c_float,
                                            c_ptr, c_ptr]),
+    "tv_attn_batched_workspace_size": (c_size, [c_i32, c_ptr, c_i32, c_i32, c_i32, c_i32]),
+    "tv_tree_attn_verify_batched": (c_i32, [c_i32, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr,
+                                            c_ptr, c_ptr, c_i32, c_i32, c_i32, c_i32,
+                                            ctypes.c_float, c_ptr, c_size, c_ptr, c_ptr]),
     "tv_tree_accept": (c_i32, [c_ptr, c_i32, c_ptr, c_ptr, c_i32, c_i32, c_ptr, c_ptr, c_ptr,
                                c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr]),
     "tv_kv_compact": (c_i32, [c_ptr, c_ptr, c_i32, c_i64, c_i32, c_i64, c_i32, c_i32, c_i32,

@@ -115,6 +115,82 @@ tv_status tv_tree_attn_verify(const void* q, const void* k_cache, const void* v_
   return from_cuda(tv::launch_combine(p, plan, ws, s));
 }
 
+size_t tv_attn_batched_workspace_size(int32_t batch, const int32_t* n_nodes, int32_t hq,
+                                      int32_t hkv, int32_t d, int32_t dtype) {
+  if (batch < 1 || batch > TV_MAX_BATCH || !n_nodes || dtype != TV_BF16) return 0;
+  for (int b = 0; b < batch; ++b)
+    if (check_attn_shape(n_nodes[b], hq, hkv, d, dtype) != TV_OK) return 0;
+  int sms = tv::device_sm_count();
+  if (sms <= 0) sms = 256;  // no device visible: an upper bound
+  tv::SplitPlan plans[TV_MAX_BATCH];
+  size_t total = 0;
+  tv::plan_attention_batched(batch, n_nodes, nullptr, hq, hkv, d, sms, plans, nullptr, &total);
+  return total;
+}
+
+tv_status tv_tree_attn_verify_batched(int32_t batch, const void* const* q,
+                                      const void* const* k_cache, const void* const* v_cache,
+                                      const int64_t* cap, const int32_t* prefix_len,
+                                      const int32_t* n_nodes, const int32_t* const* parent,
+                                      void* const* out, int32_t hq, int32_t hkv, int32_t d,
+                                      int32_t dtype, float scale, void* workspace,
+                                      size_t ws_bytes, int32_t* dev_status, tv_stream_t stream) {
+  if (batch < 1 || batch > TV_MAX_BATCH) return TV_ERR_INVALID_ARG;
+  if (!q || !k_cache || !v_cache || !cap || !prefix_len || !n_nodes || !parent || !out ||
+      !workspace)
+    return TV_ERR_INVALID_ARG;
+  if (!aligned16(workspace)) return TV_ERR_INVALID_ARG;
+  if (!(scale >= 0.f) || std::isinf(scale)) return TV_ERR_INVALID_ARG;
+  for (int b = 0; b < batch; ++b) {
+    const tv_status st = check_attn_shape(n_nodes[b], hq, hkv, d, dtype);
+    if (st != TV_OK) return st;
+    if (!q[b] || !k_cache[b] || !v_cache[b] || !parent[b] || !out[b]) return TV_ERR_INVALID_ARG;
+    if (!aligned16(q[b]) || !aligned16(k_cache[b]) || !aligned16(v_cache[b]) ||
+        !aligned16(out[b]))
+      return TV_ERR_INVALID_ARG;
+    if (prefix_len[b] < 0 || cap[b] < 1) return TV_ERR_INVALID_ARG;
+    if ((int64_t)prefix_len[b] + n_nodes[b] > cap[b]) return TV_ERR_CAPACITY;
+    if ((int64_t)prefix_len[b] + n_nodes[b] > INT32_MAX / 2) return TV_ERR_UNSUPPORTED;
+  }
+  if (dtype != TV_BF16) return TV_ERR_UNSUPPORTED;
+  const int sms = tv::device_sm_count();
+  if (sms <= 0) return TV_ERR_CUDA;
+  tv::SplitPlan plans[TV_MAX_BATCH];
+  size_t offs[TV_MAX_BATCH], total = 0;
+  tv::plan_attention_batched(batch, n_nodes, prefix_len, hq, hkv, d, sms, plans, offs, &total);
+  if (ws_bytes < total) return TV_ERR_CAPACITY;
+  const float sc = scale > 0.f ? scale : 1.0f / std::sqrt((float)d);
+  tv::AttnProblem probs[TV_MAX_BATCH];
+  float* ws[TV_MAX_BATCH];
+  for (int b = 0; b < batch; ++b) {
+    tv::AttnProblem& p = probs[b];
+    p = tv::AttnProblem{};
+    p.q = q[b];
+    p.k = k_cache[b];
+    p.v = v_cache[b];
+    p.out = out[b];
+    p.parent = parent[b];
+    p.dev_status = dev_status;
+    p.cap = cap[b];
+    p.prefix = prefix_len[b];
+    p.n = n_nodes[b];
+    p.hq = hq;
+    p.hkv = hkv;
+    p.d = d;
+    p.dtype = dtype;
+    p.scale_log2 = sc * 1.4426950408889634f;  // log2(e)
+    ws[b] = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + offs[b]);
+  }
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  if (tv::launch_attn_tc_batched(probs, plans, batch, ws, s) != cudaSuccess) return TV_ERR_CUDA;
+  for (int b = 0; b < batch; ++b)
+    if (plans[b].splits > 1) {
+      const tv_status st = from_cuda(tv::launch_combine(probs[b], plans[b], ws[b], s));
+      if (st != TV_OK) return st;
+    }
+  return TV_OK;
+}
+
 tv_status tv_tree_accept(const float* logits, int32_t vocab, const int32_t* token,
                          const int32_t* parent, int32_t n_nodes, int32_t prefix_len,
                          int32_t* am, int32_t* m, int32_t* path, int32_t* out_tokens,

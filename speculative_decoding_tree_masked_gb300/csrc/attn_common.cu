@@ -8,6 +8,7 @@
 // (log2 units: scores are pre-multiplied by scale * log2(e).)
 #include <algorithm>
 #include <cmath>
+#include <vector>
 
 #include <cuda_fp16.h>
 
@@ -73,6 +74,48 @@ SplitPlan plan_attention(int32_t n, int32_t hq, int32_t hkv, int32_t d, int32_t 
   p.ws_bytes = (partial_o_offset(p.splits, rows_all) + (size_t)p.splits * rows_all * d * o_elem +
                 255) & ~size_t(255);
   return p;
+}
+
+// Several bf16 requests in one tensor-core launch.  Each request keeps the
+// single-request row tiling; its key splits are proportional to its key
+// blocks, kblocks_b * SMs / W with W the batch's (units x key blocks), so
+// that every CTA gets about the same number of blocks and the batch fills
+// about one wave.  The workspace gives request b room for its largest
+// possible split count, max(1, SMs / units_b), whatever the prefix lengths,
+// so its layout depends only on the node counts.
+void plan_attention_batched(int batch, const int32_t* n, const int32_t* prefix, int32_t hq,
+                            int32_t hkv, int32_t d, int sm_count, SplitPlan* plans,
+                            size_t* ws_offset, size_t* ws_total) {
+  const int sms = std::max(1, sm_count);
+  int64_t total_units = 0, work = 0;
+  std::vector<int64_t> units(batch), kblocks(batch);
+  for (int b = 0; b < batch; ++b) {
+    const int rows = (hq / hkv) * n[b];
+    const int tiles = (rows + kTcRowsPerTile - 1) / kTcRowsPerTile;
+    plans[b] = SplitPlan{};
+    plans[b].row_tiles = tiles <= 1 ? 1 : (tiles + 1) / 2;
+    units[b] = (int64_t)hkv * plans[b].row_tiles;
+    kblocks[b] = prefix ? ((int64_t)prefix[b] + n[b] + kTcKeys - 1) / kTcKeys : 1;
+    total_units += units[b];
+    work += units[b] * kblocks[b];
+  }
+  size_t off = 0;
+  for (int b = 0; b < batch; ++b) {
+    int64_t s = 1;
+    if (prefix && total_units < sms) s = std::max<int64_t>(1, kblocks[b] * sms / work);
+    s = std::min<int64_t>(s, kblocks[b]);
+    const int64_t per = (kblocks[b] + s - 1) / s;
+    plans[b].keys_per_split = (int32_t)(per * kTcKeys);
+    plans[b].splits = (int32_t)((kblocks[b] + per - 1) / per);
+    const int64_t s_max = std::max<int64_t>(1, sms / units[b]);
+    const size_t rows_all = (size_t)n[b] * hq;
+    const size_t bytes = (partial_o_offset((int)s_max, rows_all) +
+                          (size_t)s_max * rows_all * d * 2 + 255) & ~size_t(255);
+    plans[b].ws_bytes = bytes;
+    if (ws_offset) ws_offset[b] = off;
+    off += bytes;
+  }
+  if (ws_total) *ws_total = off;
 }
 
 __device__ __forceinline__ void load_partial(const float* p, float (&o)[4]) {

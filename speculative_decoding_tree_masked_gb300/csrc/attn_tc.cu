@@ -90,6 +90,23 @@ struct TcParams {
   float scale_log2;
 };
 
+// Kernel argument: up to MAXB requests, each with its tensor maps (K, V, Q,
+// output) and parameters.  With MAXB == 1 the grid is (splits, row groups,
+// KV heads); with several requests the grid is one-dimensional and cta[]
+// names each CTA's (request, KV head, row group, split).
+constexpr int kMaxBatchCtas = 2048;
+
+__host__ __device__ constexpr uint32_t pack_cta(int b, int g, int rg, int split) {
+  return ((uint32_t)b << 28) | ((uint32_t)g << 20) | ((uint32_t)rg << 12) | (uint32_t)split;
+}
+
+template <int MAXB>
+struct TcBatch {
+  CUtensorMap kmap[MAXB], vmap[MAXB], qmap[MAXB], omap[MAXB];
+  TcParams req[MAXB];
+  uint32_t cta[MAXB == 1 ? 1 : kMaxBatchCtas];
+};
+
 template <int D>
 struct Layout {
   static constexpr uint32_t kQTile = kBM * D * 2;   // bytes of one Q tile
@@ -177,21 +194,35 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int D>
+template <int D, int MAXB>
 __global__ void __launch_bounds__(kThreads, 1)
-attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-               const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
-               const TcParams p) {
+attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
   using L = Layout<D>;
+  int b = 0, split, g, rgroup;
+  if (MAXB == 1) {
+    split = blockIdx.x;
+    rgroup = blockIdx.y;
+    g = blockIdx.z;
+  } else {
+    const uint32_t e = batch.cta[blockIdx.x];
+    b = (int)(e >> 28);
+    g = (int)((e >> 20) & 0xffu);
+    rgroup = (int)((e >> 12) & 0xffu);
+    split = (int)(e & 0xfffu);
+  }
+  const TcParams& p = batch.req[b];
+  const CUtensorMap* kmap = &batch.kmap[b];
+  const CUtensorMap* vmap = &batch.vmap[b];
+  const CUtensorMap* qmap = &batch.qmap[b];
+  const CUtensorMap* omap = &batch.omap[b];
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* sm = smem_raw + (base - raw);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x, g = blockIdx.z;
   const int G = p.hq / p.hkv;
-  const int row0 = blockIdx.y * (kTiles * kBM);
+  const int row0 = rgroup * (kTiles * kBM);
   const int ntiles = min(kTiles, (p.rows_per_head - row0 + kBM - 1) / kBM);
   const int kbeg = split * p.keys_per_split;
   const int kend = min(p.keys, kbeg + p.keys_per_split);
@@ -233,7 +264,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     ptx::mbar_arrive_expect_tx(bars.k_full(s), L::kKV);
 #pragma unroll
     for (int c = 0; c < D / 64; ++c)
-      ptx::tma_load_3d(base + L::kK + s * L::kKV + c * (kBN * 128), &kmap, bars.k_full(s), c * 64,
+      ptx::tma_load_3d(base + L::kK + s * L::kKV + c * (kBN * 128), kmap, bars.k_full(s), c * 64,
                        kbeg + j * kBN, g);
   };
   auto load_v = [&](int j) {
@@ -241,7 +272,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     ptx::mbar_arrive_expect_tx(bars.v_full(s), L::kKV);
 #pragma unroll
     for (int c = 0; c < D / 64; ++c)
-      ptx::tma_load_3d(base + L::kV + s * L::kKV + c * (kBN * 128), &vmap, bars.v_full(s), c * 64,
+      ptx::tma_load_3d(base + L::kV + s * L::kKV + c * (kBN * 128), vmap, bars.v_full(s), c * 64,
                        kbeg + j * kBN, g);
   };
   if (warp == 1) {
@@ -256,7 +287,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     for (int t = 0; t < ntiles; ++t)
 #pragma unroll
       for (int c = 0; c < D / 64; ++c)
-        ptx::tma_load_3d(base + L::kQ + t * L::kQTile + c * (kBM * 128), &qmap, bars.q_full(),
+        ptx::tma_load_3d(base + L::kQ + t * L::kQTile + c * (kBM * 128), qmap, bars.q_full(),
                          c * 64, g * G, (row0 + t * kBM) / G);
   }
   if (tid == 0 && nb > 0) load_k(0);  // V_0 follows once K_0 has landed
@@ -649,7 +680,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             wait_bar(bars.epi(t), 0, abort_flag, p.dev_status)) {
 #pragma unroll
           for (int cc = 0; cc < D / 64; ++cc)
-            ptx::tma_store_4d(&omap, base + L::kQ + t * L::kQTile + cc * (kBM * 128), cc * 64,
+            ptx::tma_store_4d(omap, base + L::kQ + t * L::kQTile + cc * (kBM * 128), cc * 64,
                               g * G, (row0 + t * kBM) / G, to_out ? 0 : split);
           ptx::bulk_commit_group();
           ptx::bulk_wait_group_read0();
@@ -745,55 +776,99 @@ bool make_q_map(CUtensorMap* map, const void* base, int d, int n, int hq, int gr
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
-cudaError_t launch_d(const AttnProblem& p, const SplitPlan& plan, float* ws, cudaStream_t s) {
+template <int D, int MAXB>
+cudaError_t set_smem_attr() {
   static bool attr_set[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_tc_kernel<D, MAXB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)Layout<D>::kAlloc);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  CUtensorMap kmap, vmap, qmap, omap;
+  return cudaSuccess;
+}
+
+// The tensor maps and parameters of one request under its split plan.
+template <int D>
+bool fill_request(const AttnProblem& p, const SplitPlan& plan, float* ws, CUtensorMap* kmap,
+                  CUtensorMap* vmap, CUtensorMap* qmap, CUtensorMap* omap, TcParams* tp) {
   const int rows = p.prefix + p.n;
-  if (!make_kv_map(&kmap, p.k, D, rows, p.cap, p.hkv) ||
-      !make_kv_map(&vmap, p.v, D, rows, p.cap, p.hkv))
-    return cudaErrorInvalidValue;
+  if (!make_kv_map(kmap, p.k, D, rows, p.cap, p.hkv) ||
+      !make_kv_map(vmap, p.v, D, rows, p.cap, p.hkv))
+    return false;
   const int group = p.hq / p.hkv;
   const bool q_tma = (kBM % group) == 0;
-  if (q_tma && !make_q_map(&qmap, p.q, D, p.n, p.hq, group)) return cudaErrorInvalidValue;
-  if (!q_tma) memset(&qmap, 0, sizeof(qmap));
+  if (q_tma && !make_q_map(qmap, p.q, D, p.n, p.hq, group)) return false;
+  if (!q_tma) memset(qmap, 0, sizeof(*qmap));
   if (q_tma) {
     const bool to_out = plan.splits == 1;
     void* obase = to_out ? p.out
                          : static_cast<void*>(reinterpret_cast<uint8_t*>(ws) +
                                               partial_o_offset(plan.splits, (size_t)p.n * p.hq));
-    if (!make_o_map(&omap, obase, !to_out, D, p.n, p.hq, group, to_out ? 1 : plan.splits))
-      return cudaErrorInvalidValue;
+    if (!make_o_map(omap, obase, !to_out, D, p.n, p.hq, group, to_out ? 1 : plan.splits))
+      return false;
   } else {
-    memset(&omap, 0, sizeof(omap));
+    memset(omap, 0, sizeof(*omap));
   }
-  TcParams tp{};
-  tp.q = static_cast<const __nv_bfloat16*>(p.q);
-  tp.out = static_cast<__nv_bfloat16*>(p.out);
-  tp.ws = ws;
-  tp.parent = p.parent;
-  tp.dev_status = p.dev_status;
-  tp.n = p.n;
-  tp.hq = p.hq;
-  tp.hkv = p.hkv;
-  tp.prefix = p.prefix;
-  tp.keys = rows;
-  tp.keys_per_split = plan.keys_per_split;
-  tp.splits = plan.splits;
-  tp.rows_per_head = (p.hq / p.hkv) * p.n;
-  tp.scale_log2 = p.scale_log2;
-  tp.q_tma = q_tma ? 1 : 0;
+  *tp = TcParams{};
+  tp->q = static_cast<const __nv_bfloat16*>(p.q);
+  tp->out = static_cast<__nv_bfloat16*>(p.out);
+  tp->ws = ws;
+  tp->parent = p.parent;
+  tp->dev_status = p.dev_status;
+  tp->n = p.n;
+  tp->hq = p.hq;
+  tp->hkv = p.hkv;
+  tp->prefix = p.prefix;
+  tp->keys = rows;
+  tp->keys_per_split = plan.keys_per_split;
+  tp->splits = plan.splits;
+  tp->rows_per_head = (p.hq / p.hkv) * p.n;
+  tp->scale_log2 = p.scale_log2;
+  tp->q_tma = q_tma ? 1 : 0;
+  return true;
+}
+
+template <int D>
+cudaError_t launch_d(const AttnProblem& p, const SplitPlan& plan, float* ws, cudaStream_t s) {
+  cudaError_t e = set_smem_attr<D, 1>();
+  if (e != cudaSuccess) return e;
+  TcBatch<1> batch;
+  memset(&batch, 0, sizeof(batch));
+  if (!fill_request<D>(p, plan, ws, &batch.kmap[0], &batch.vmap[0], &batch.qmap[0],
+                       &batch.omap[0], &batch.req[0]))
+    return cudaErrorInvalidValue;
   const dim3 grid(plan.splits, plan.row_tiles, p.hkv);
-  attn_tc_kernel<D><<<grid, kThreads, Layout<D>::kAlloc, s>>>(kmap, vmap, qmap, omap, tp);
+  attn_tc_kernel<D, 1><<<grid, kThreads, Layout<D>::kAlloc, s>>>(batch);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_batched_d(const AttnProblem* probs, const SplitPlan* plans, int batch_n,
+                             float* const* ws, cudaStream_t s) {
+  cudaError_t e = set_smem_attr<D, kMaxBatch>();
+  if (e != cudaSuccess) return e;
+  // about 13 KB: built on the heap, passed by value to the launch
+  auto* batch = new TcBatch<kMaxBatch>;
+  memset(batch, 0, sizeof(*batch));
+  int ctas = 0;
+  bool ok = batch_n <= kMaxBatch;
+  for (int b = 0; ok && b < batch_n; ++b) {
+    ok = fill_request<D>(probs[b], plans[b], ws[b], &batch->kmap[b], &batch->vmap[b],
+                         &batch->qmap[b], &batch->omap[b], &batch->req[b]);
+    for (int g = 0; ok && g < probs[b].hkv; ++g)
+      for (int rg = 0; ok && rg < plans[b].row_tiles; ++rg)
+        for (int sp = 0; ok && sp < plans[b].splits; ++sp) {
+          ok = ctas < kMaxBatchCtas && g < 256 && rg < 256 && sp < 4096;
+          if (ok) batch->cta[ctas++] = pack_cta(b, g, rg, sp);
+        }
+  }
+  if (ok) attn_tc_kernel<D, kMaxBatch><<<ctas, kThreads, Layout<D>::kAlloc, s>>>(*batch);
+  delete batch;
+  if (!ok) return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 
@@ -802,6 +877,13 @@ cudaError_t launch_d(const AttnProblem& p, const SplitPlan& plan, float* ws, cud
 cudaError_t launch_attn_tc(const AttnProblem& p, const SplitPlan& plan, float* ws,
                            cudaStream_t s) {
   return p.d == 128 ? launch_d<128>(p, plan, ws, s) : launch_d<64>(p, plan, ws, s);
+}
+
+cudaError_t launch_attn_tc_batched(const AttnProblem* probs, const SplitPlan* plans,
+                                   int batch_n, float* const* ws, cudaStream_t s) {
+  if (batch_n < 1) return cudaErrorInvalidValue;
+  return probs[0].d == 128 ? launch_batched_d<128>(probs, plans, batch_n, ws, s)
+                           : launch_batched_d<64>(probs, plans, batch_n, ws, s);
 }
 
 }  // namespace tv

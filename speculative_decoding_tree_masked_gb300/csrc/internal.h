@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "treeverify.h"
+
 namespace tv {
 
 struct AttnProblem {
@@ -55,6 +57,15 @@ cudaError_t launch_attn_simt(const AttnProblem& p, const SplitPlan& plan, float*
                              cudaStream_t s);
 cudaError_t launch_attn_tc(const AttnProblem& p, const SplitPlan& plan, float* ws,
                            cudaStream_t s);
+void plan_attention_batched(int batch, const int32_t* n, const int32_t* prefix, int32_t hq,
+                            int32_t hkv, int32_t d, int sm_count, SplitPlan* plans,
+                            size_t* ws_offset, size_t* ws_total);
+
+// Several requests in one launch of the tensor-core kernel (bf16): request b
+// under plans[b] with its partials at ws[b].
+constexpr int kMaxBatch = TV_MAX_BATCH;
+cudaError_t launch_attn_tc_batched(const AttnProblem* probs, const SplitPlan* plans,
+                                   int batch_n, float* const* ws, cudaStream_t s);
 cudaError_t launch_combine(const AttnProblem& p, const SplitPlan& plan, const float* ws,
                            cudaStream_t s);
 

@@ -136,3 +136,33 @@ def test_sampled_accept_host_checks(lib):
     assert call(T=float("nan")) == 1
     assert call(n=0) == 1
     assert call(V=0) == 1
+
+
+def test_batched_attention_host_checks(lib):
+    import ctypes
+    fake = ctypes.c_void_p(0x1000)
+    B = 2
+
+    def arr(ctype, vals):
+        return ctypes.cast((ctype * len(vals))(*vals), ctypes.c_void_p)
+
+    def call(batch=B, n=(5, 7), P=(10, 20), cap=(100, 100), dt=1, d=128, hq=8, hkv=2,
+             ptrs=None, ws=0x1000, wsb=1 << 30):
+        ptrs = ptrs or [0x1000, 0x2000]
+        vp = arr(ctypes.c_void_p, ptrs[:max(batch, 1)] + [0x3000] * max(0, batch - 2))
+        nn = arr(ctypes.c_int32, list(n) + [5] * max(0, batch - 2))
+        pp = arr(ctypes.c_int32, list(P) + [0] * max(0, batch - 2))
+        cc = arr(ctypes.c_int64, list(cap) + [100] * max(0, batch - 2))
+        return lib.tv_tree_attn_verify_batched(batch, vp, vp, vp, cc, pp, nn, vp, vp, hq, hkv,
+                                               d, dt, 0.0, ctypes.c_void_p(ws), wsb, None, None)
+    assert call(batch=0) == 1
+    assert call(batch=17) == 1
+    assert call(n=(5, 200)) == 1
+    assert call(cap=(100, 12)) == 3                   # request 1 cannot hold its tree
+    assert call(ptrs=[0x1000, 0x2004]) == 1           # misaligned
+    assert call(d=96) == 2
+    assert call(dt=0) == 2                            # fp32 has no batched kernel
+    ns = (ctypes.c_int32 * 2)(64, 8)
+    assert lib.tv_attn_batched_workspace_size(2, ctypes.cast(ns, ctypes.c_void_p), 64, 8, 128, 1) > 0
+    assert lib.tv_attn_batched_workspace_size(2, ctypes.cast(ns, ctypes.c_void_p), 64, 8, 128, 0) == 0
+    assert lib.tv_attn_batched_workspace_size(0, ctypes.cast(ns, ctypes.c_void_p), 64, 8, 128, 1) == 0
