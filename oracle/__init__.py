@@ -14,6 +14,7 @@ from .tree_verify import (  # noqa: F401
 from .tree_expand import (  # noqa: F401
     candidate_scores, draft_reroot, log_softmax, ml_expand,
 )
+from .lm_head import lm_head_argmax, lm_head_logits  # noqa: F401
 from .tree_sample import (  # noqa: F401
     draw_by_inversion, node_uniform, philox4x64_10, sample_tokens, target_probs,
     tree_accept_sampled,
