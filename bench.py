@@ -750,6 +750,87 @@ def run_batch(args, local_rank):
         "peak_source": peaks["source"]}), flush=True)
 
 
+def run_lmhead(args, local_rank):
+    """The target's LM head fused with the argmax at Llama-3-70B shapes
+    (d_model 8192, vocabulary 128256, bf16 weights: 2.1 GB, larger than L2)
+    for one 64-node tree and for four trees at once (256 nodes), then the
+    greedy walk fed with its tokens.  The cuBLAS GEMM that would write the
+    logits instead is timed beside it for context.  One JSON line."""
+    import torch
+
+    import speculative_decoding_tree_masked_gb300 as tvp
+    from workloads import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.Stream(dev)
+    peaks = _peaks()
+    d_model = 8192
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(args.seed)
+    weight = (torch.randn(VOCAB, d_model, device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+    w = synth.make_workload(WORKLOAD, seed=args.seed, layers=1)
+    token = torch.from_numpy(w.token).to(dev)
+    parent = torch.from_numpy(w.parent).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    reps = max(3, args.steps)
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            fn()
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                graph.replay()
+            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ea.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            eb.record(stream)
+        torch.cuda.synchronize()
+        return ea.elapsed_time(eb) * 1e3 / reps
+
+    out = {}
+    for n in (NODES, 4 * NODES):
+        hidden = torch.randn(n, d_model, device=dev, generator=gen).to(torch.bfloat16)
+        ws = tvp.lm_head_workspace(n, VOCAB, dev)
+        res = {"am": torch.empty(n, dtype=torch.int32, device=dev),
+               "max_logit": torch.empty(n, dtype=torch.float32, device=dev)}
+        us = timed(lambda: tvp.lm_head_argmax(hidden, weight, outs=res, workspace=ws,
+                                              status=status))
+        nbytes = VOCAB * d_model * 2 + n * d_model * 2
+        gemm_us = timed(lambda: torch.matmul(hidden, weight.t()))
+        out[n] = {"us": us, "bytes": nbytes, "gbs": nbytes / us / 1e3,
+                  "hbm_frac": nbytes / us / 1e3 / peaks["hbm_gbs"],
+                  "tflops": 2.0 * n * d_model * VOCAB / us / 1e6, "cublas_gemm_us": gemm_us}
+        if n == NODES:
+            acc = {k: torch.empty(sz, dtype=torch.int32, device=dev) for k, sz in (
+                ("m", 1), ("path", n), ("out_tokens", n + 1), ("new_pos", n),
+                ("new_parent", n), ("n_survivors", 1))}
+
+            def fused():
+                tvp.lm_head_argmax(hidden, weight, outs=res, workspace=ws, status=status)
+                tvp.tree_accept_tokens(res["am"], VOCAB, token, parent, PREFIX, outs=acc,
+                                       status=status)
+            out["with_walk_us"] = timed(fused)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the LM head")
+    a, b = out[NODES], out[4 * NODES]
+    print(json.dumps({
+        "kernel": "LM head fused with the argmax (tcgen05 GEMM, argmax epilogue)",
+        "workload": f"{NODES} tree nodes x d_model {d_model} x vocab {VOCAB} (bf16 weights)",
+        "us_per_call": a["us"], "hbm_gbs": a["gbs"], "hbm_frac": a["hbm_frac"],
+        "bytes": a["bytes"], "tensor_tflops": a["tflops"],
+        "with_greedy_walk_us": out["with_walk_us"],
+        "cublas_logits_gemm_us": a["cublas_gemm_us"],
+        "nodes_256": {"us_per_call": b["us"], "hbm_frac": b["hbm_frac"],
+                      "tensor_tflops": b["tflops"], "cublas_logits_gemm_us": b["cublas_gemm_us"]},
+        "l2": "weights (2.1 GB) larger than L2", "peak_source": peaks["source"]}), flush=True)
+
+
 def _splits_for(tvp, n, hq, hkv, d, prefix):
     import torch
     nbytes = tvp.attn_workspace_size(n, hq, hkv, d, torch.bfloat16, prefix)
@@ -782,6 +863,8 @@ def main():
                     help="time greedy and sampling acceptance instead of the step")
     ap.add_argument("--expand", action="store_true",
                     help="time the draft side's tree expansion instead of the step")
+    ap.add_argument("--lmhead", action="store_true",
+                    help="time the LM head fused with the argmax instead of the step")
     ap.add_argument("--sweep", action="store_true",
                     help="time the attention alone over the prefix x tree-size sweep "
                          "(one JSON line per configuration) instead of the step")
@@ -794,10 +877,10 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
-    if args.sweep or args.expand or args.sample or args.batch:
+    if args.sweep or args.expand or args.sample or args.batch or args.lmhead:
         if rank == 0:
             mode = (run_sweep if args.sweep else run_expand if args.expand else
-                    run_sample if args.sample else run_batch)
+                    run_sample if args.sample else run_lmhead if args.lmhead else run_batch)
             mode(args, local_rank)
         return
     if world > 1:

@@ -272,6 +272,25 @@ TV_API tv_status tv_tree_accept(const float* logits, int32_t vocab, const int32_
                          int32_t* dev_status, tv_stream_t stream);
 
 /*
+ * tv_tree_accept_tokens -- tv_tree_accept without the argmax pass: the
+ * target's token at every node is given (am of tv_lm_head_argmax, which
+ * never writes the logits).  Same passage and outputs as tv_tree_accept,
+ * less am.
+ *
+ *   target_token  device int32 [n_nodes]: the target's token at each node
+ *                 (a value outside [0, vocab) matches no draft token; it is
+ *                 still emitted as the bonus token when the walk stops there)
+ *   vocab, token, parent, n_nodes, prefix_len, outputs, dev_status: as for
+ *                 tv_tree_accept
+ */
+TV_API tv_status tv_tree_accept_tokens(const int32_t* target_token, int32_t vocab,
+                                       const int32_t* token, const int32_t* parent,
+                                       int32_t n_nodes, int32_t prefix_len, int32_t* m,
+                                       int32_t* path, int32_t* out_tokens, int32_t* new_pos,
+                                       int32_t* new_parent, int32_t* n_survivors,
+                                       int32_t* dev_status, tv_stream_t stream);
+
+/*
  * tv_tree_accept_sampled -- sampling (stochastic) verification of the draft
  * tree at temperature T, with the outputs of tv_tree_accept.
  *
@@ -430,6 +449,50 @@ TV_API tv_status tv_draft_reroot(const int32_t* parent, const int32_t* token, co
                                  int32_t* new_pos, int32_t* new_parent, int32_t* new_token,
                                  float* new_cum, int32_t* n_survivors, int32_t* dev_status,
                                  tv_stream_t stream);
+
+/*
+ * The target's LM head fused with the argmax.
+ */
+
+#define TV_MAX_LM_NODES 256
+
+/* Bytes of workspace tv_lm_head_argmax needs on the current device; 0 for
+ * arguments it rejects. */
+TV_API size_t tv_lm_head_workspace_size(int32_t n_nodes, int32_t vocab);
+
+/*
+ * tv_lm_head_argmax -- the target's greedy token at every tree node, straight
+ * from the final hidden states.
+ *
+ * Passage: SwiftSpec review page, "What carries the argument" (the verified
+ * tokens are the target's greedy choices at the tree nodes); the logits the
+ * greedy walk compares are the LM head's, z_i = W h_i.  This call computes
+ *     am[i] = argmax_v  sum_k hidden[i][k] * weight[v][k]
+ * (ties to the lowest v) on the tensor cores with fp32 accumulation, and
+ * never writes the n_nodes x vocab logits to memory.  am feeds the greedy
+ * walk in place of tv_tree_accept's own argmax pass.
+ *
+ *   hidden     device bf16 [n_nodes][d_model], rows contiguous, 16-byte
+ *              aligned: the final (normalised) hidden state of each node
+ *   weight     device bf16 [vocab][d_model], rows contiguous, 16-byte
+ *              aligned: the LM head (the layout of a linear layer's weight)
+ *   n_nodes    1 .. TV_MAX_LM_NODES
+ *   d_model    a multiple of 8, at least 8
+ *   vocab      >= 1
+ * Outputs (device, written):
+ *   am         int32 [n_nodes]    the argmax token of each node
+ *   max_logit  float32 [n_nodes]  its fp32 logit; may be NULL
+ * workspace: device memory of at least tv_lm_head_workspace_size bytes,
+ * 16-byte aligned; its contents on entry do not matter.  dev_status: device
+ * int32 or NULL; TV_ERR_TIMEOUT if a device wait ran out (outputs are then
+ * unspecified).  Logits are rounded float32 sums, so tokens whose exact
+ * logits differ by less than that rounding may be chosen either way; a node
+ * whose logits are all NaN or -inf gets -1.
+ */
+TV_API tv_status tv_lm_head_argmax(const void* hidden, const void* weight, int32_t n_nodes,
+                                   int32_t d_model, int32_t vocab, int32_t* am, float* max_logit,
+                                   void* workspace, size_t ws_bytes, int32_t* dev_status,
+                                   tv_stream_t stream);
 
 #ifdef __cplusplus
 }

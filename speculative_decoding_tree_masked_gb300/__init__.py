@@ -221,6 +221,32 @@ def tree_accept(logits: torch.Tensor, token: torch.Tensor, parent: torch.Tensor,
     return outs
 
 
+def tree_accept_tokens(target_token: torch.Tensor, vocab: int, token: torch.Tensor,
+                       parent: torch.Tensor, prefix_len: int, outs: Optional[dict] = None,
+                       status: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """tree_accept with the target's token at every node given (the "am" of
+    lm_head_argmax) instead of logits.  Returns the dict of tree_accept
+    without "am"."""
+    _need_cuda(target_token, token, parent)
+    n = parent.numel()
+    if target_token.dtype != torch.int32 or token.dtype != torch.int32 or \
+            parent.dtype != torch.int32:
+        raise ValueError("dtype mismatch")
+    if token.numel() != n or target_token.numel() != n:
+        raise ValueError("shape mismatch")
+    if outs is None:
+        dev = parent.device
+        outs = {k: torch.empty(sz, dtype=torch.int32, device=dev) for k, sz in (
+            ("m", 1), ("path", n), ("out_tokens", n + 1), ("new_pos", n), ("new_parent", n),
+            ("n_survivors", 1))}
+    _check(lib().tv_tree_accept_tokens(
+        _ptr(target_token), vocab, _ptr(token), _ptr(parent), n, prefix_len, _ptr(outs["m"]),
+        _ptr(outs["path"]), _ptr(outs["out_tokens"]), _ptr(outs["new_pos"]),
+        _ptr(outs["new_parent"]), _ptr(outs["n_survivors"]), _ptr(status),
+        _stream(stream, parent.device)), "tv_tree_accept_tokens")
+    return outs
+
+
 def tree_accept_sampled(logits: torch.Tensor, token: torch.Tensor, parent: torch.Tensor,
                         prefix_len: int, temperature: float, seed: int, offset: int,
                         outs: Optional[dict] = None, status: Optional[torch.Tensor] = None,
@@ -304,6 +330,44 @@ def tree_expand(logits: torch.Tensor, frontier: torch.Tensor, cum: torch.Tensor,
         _ptr(outs["token"]), _ptr(outs["score"]), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(status),
         _stream(stream, logits.device)), "tv_tree_expand")
+    return outs
+
+
+def lm_head_workspace(n_nodes: int, vocab: int, device) -> torch.Tensor:
+    """A workspace for lm_head_argmax (bytes, 16-byte aligned)."""
+    nbytes = int(lib().tv_lm_head_workspace_size(n_nodes, vocab))
+    if nbytes == 0:
+        raise TreeVerifyError(TV_ERR_INVALID_ARG, "tv_lm_head_workspace_size")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def lm_head_argmax(hidden: torch.Tensor, weight: torch.Tensor, outs: Optional[dict] = None,
+                   workspace: Optional[torch.Tensor] = None,
+                   status: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """The target's greedy token at every tree node from its final hidden
+    state: am[i] = argmax_v hidden[i] . weight[v] (lowest v on ties), the
+    logits never written out.  hidden bf16 [N][d_model], weight bf16
+    [V][d_model] (both contiguous).  Returns (or fills) a dict of device
+    tensors am int32 [N] and max_logit float32 [N]."""
+    _need_cuda(hidden, weight)
+    if hidden.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
+        raise ValueError("hidden and weight must be bfloat16")
+    if hidden.dim() != 2 or weight.dim() != 2 or hidden.shape[1] != weight.shape[1]:
+        raise ValueError("shape mismatch")
+    if not hidden.is_contiguous() or not weight.is_contiguous():
+        raise ValueError("hidden and weight must be contiguous")
+    n, d = hidden.shape
+    vocab = weight.shape[0]
+    if outs is None:
+        dev = hidden.device
+        outs = {"am": torch.empty(n, dtype=torch.int32, device=dev),
+                "max_logit": torch.empty(n, dtype=torch.float32, device=dev)}
+    if workspace is None:
+        workspace = lm_head_workspace(n, vocab, hidden.device)
+    _check(lib().tv_lm_head_argmax(
+        _ptr(hidden), _ptr(weight), n, d, vocab, _ptr(outs["am"]), _ptr(outs.get("max_logit")),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
+        _stream(stream, hidden.device)), "tv_lm_head_argmax")
     return outs
 
 

@@ -37,6 +37,8 @@ SIGNATURES = {
                                c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr]),
     "tv_kv_compact": (c_i32, [c_ptr, c_ptr, c_i32, c_i64, c_i32, c_i64, c_i32, c_i32, c_i32,
                               c_i32, c_ptr, c_ptr, c_ptr]),
+    "tv_tree_accept_tokens": (c_i32, [c_ptr, c_i32, c_ptr, c_ptr, c_i32, c_i32, c_ptr, c_ptr,
+                                      c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr]),
     "tv_tree_accept_sampled": (c_i32, [c_ptr, c_i32, c_ptr, c_ptr, c_i32, c_i32, ctypes.c_float,
                                        ctypes.c_uint64, ctypes.c_uint64, c_ptr, c_ptr, c_ptr,
                                        c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr]),
@@ -45,6 +47,9 @@ SIGNATURES = {
                                c_ptr, c_ptr, c_size, c_ptr, c_ptr]),
     "tv_draft_reroot": (c_i32, [c_ptr, c_ptr, c_ptr, c_i32, c_ptr, c_ptr, c_ptr, c_i32, c_ptr,
                                 c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr]),
+    "tv_lm_head_workspace_size": (c_size, [c_i32, c_i32]),
+    "tv_lm_head_argmax": (c_i32, [c_ptr, c_ptr, c_i32, c_i32, c_i32, c_ptr, c_ptr, c_ptr, c_size,
+                                  c_ptr, c_ptr]),
 }
 
 _lib = None

@@ -208,6 +208,22 @@ tv_status tv_tree_accept(const float* logits, int32_t vocab, const int32_t* toke
                                      dev_status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+tv_status tv_tree_accept_tokens(const int32_t* target_token, int32_t vocab, const int32_t* token,
+                                const int32_t* parent, int32_t n_nodes, int32_t prefix_len,
+                                int32_t* m, int32_t* path, int32_t* out_tokens, int32_t* new_pos,
+                                int32_t* new_parent, int32_t* n_survivors, int32_t* dev_status,
+                                tv_stream_t stream) {
+  if (!target_token || !token || !parent || !m || !path || !out_tokens || !new_pos ||
+      !new_parent || !n_survivors)
+    return TV_ERR_INVALID_ARG;
+  if (vocab < 1 || n_nodes < 1 || n_nodes > TV_MAX_NODES || prefix_len < 0)
+    return TV_ERR_INVALID_ARG;
+  if ((int64_t)prefix_len + n_nodes > INT32_MAX) return TV_ERR_INVALID_ARG;
+  return from_cuda(tv::launch_walk(token, parent, target_token, n_nodes, vocab, prefix_len, m,
+                                   path, out_tokens, new_pos, new_parent, n_survivors,
+                                   dev_status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 tv_status tv_tree_accept_sampled(const float* logits, int32_t vocab, const int32_t* token,
                                  const int32_t* parent, int32_t n_nodes, int32_t prefix_len,
                                  float temperature, uint64_t seed, uint64_t offset,
@@ -292,6 +308,26 @@ tv_status tv_draft_reroot(const int32_t* parent, const int32_t* token, const flo
                                            prefix_len, new_pos, new_parent, new_token, new_cum,
                                            n_survivors, dev_status,
                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t tv_lm_head_workspace_size(int32_t n_nodes, int32_t vocab) {
+  if (n_nodes < 1 || n_nodes > TV_MAX_LM_NODES || vocab < 1) return 0;
+  return tv::lm_head_workspace_bytes(n_nodes, vocab, tv::device_sm_count());
+}
+
+tv_status tv_lm_head_argmax(const void* hidden, const void* weight, int32_t n_nodes,
+                            int32_t d_model, int32_t vocab, int32_t* am, float* max_logit,
+                            void* workspace, size_t ws_bytes, int32_t* dev_status,
+                            tv_stream_t stream) {
+  if (!hidden || !weight || !am || !workspace) return TV_ERR_INVALID_ARG;
+  if (n_nodes < 1 || n_nodes > TV_MAX_LM_NODES || vocab < 1) return TV_ERR_INVALID_ARG;
+  if (d_model < 8 || d_model % 8 != 0) return TV_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(workspace)) return TV_ERR_INVALID_ARG;
+  if (ws_bytes < tv::lm_head_workspace_bytes(n_nodes, vocab, tv::device_sm_count()))
+    return TV_ERR_CAPACITY;
+  return from_cuda(tv::launch_lm_head_argmax(hidden, weight, n_nodes, d_model, vocab, am,
+                                             max_logit, workspace, dev_status,
+                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -1,6 +1,8 @@
 // Launchers behind the C ABI (host side).
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -8,6 +10,9 @@
 #include "treeverify.h"
 
 namespace tv {
+
+// The driver's tensor-map encoder (null when the driver does not offer it).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
 
 struct AttnProblem {
   const void* q;
@@ -110,5 +115,11 @@ cudaError_t launch_compact(void* k, void* v, int32_t layers, int64_t layer_strid
                            int32_t hkv, int64_t cap, int32_t row_bytes, int32_t prefix,
                            int32_t n, const int32_t* new_pos, int32_t* dev_status,
                            cudaStream_t s);
+
+// The target's LM head fused with the argmax (bf16 hidden states and weights).
+size_t lm_head_workspace_bytes(int32_t n, int32_t vocab, int sm_count);
+cudaError_t launch_lm_head_argmax(const void* hidden, const void* weight, int32_t n,
+                                  int32_t d_model, int32_t vocab, int32_t* am, float* max_logit,
+                                  void* ws, int32_t* dev_status, cudaStream_t s);
 
 }  // namespace tv

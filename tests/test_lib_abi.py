@@ -166,3 +166,43 @@ def test_batched_attention_host_checks(lib):
     assert lib.tv_attn_batched_workspace_size(2, ctypes.cast(ns, ctypes.c_void_p), 64, 8, 128, 1) > 0
     assert lib.tv_attn_batched_workspace_size(2, ctypes.cast(ns, ctypes.c_void_p), 64, 8, 128, 0) == 0
     assert lib.tv_attn_batched_workspace_size(0, ctypes.cast(ns, ctypes.c_void_p), 64, 8, 128, 1) == 0
+
+
+def test_lm_head_host_checks(lib):
+    import ctypes
+    fake = ctypes.c_void_p(0x1000)
+    assert lib.tv_lm_head_workspace_size(64, 128256) > 0
+    assert lib.tv_lm_head_workspace_size(0, 1000) == 0
+    assert lib.tv_lm_head_workspace_size(257, 1000) == 0            # above TV_MAX_LM_NODES
+    assert lib.tv_lm_head_workspace_size(4, 0) == 0
+
+    def call(**kw):
+        a = dict(h=fake, w=fake, n=4, d=64, V=1000, am=fake, ws=fake, wsb=1 << 30)
+        a.update(kw)
+        return lib.tv_lm_head_argmax(a["h"], a["w"], a["n"], a["d"], a["V"], a["am"], None,
+                                     a["ws"], a["wsb"], None, None)
+    assert call(h=None) == 1
+    assert call(am=None) == 1
+    assert call(n=0) == 1
+    assert call(n=257) == 1
+    assert call(d=12) == 1                                           # not a multiple of 8
+    assert call(d=0) == 1
+    assert call(V=0) == 1
+    assert call(w=ctypes.c_void_p(0x1008)) == 1                      # misaligned weights
+    assert call(wsb=8) == 3                                          # workspace too small
+
+
+def test_accept_tokens_host_checks(lib):
+    import ctypes
+    fake = ctypes.c_void_p(0x1000)
+
+    def call(**kw):
+        a = dict(tt=fake, V=100, n=4, P=0)
+        a.update(kw)
+        return lib.tv_tree_accept_tokens(a["tt"], a["V"], fake, fake, a["n"], a["P"], fake, fake,
+                                         fake, fake, fake, fake, None, None)
+    assert call(tt=None) == 1
+    assert call(V=0) == 1
+    assert call(n=0) == 1
+    assert call(n=129) == 1
+    assert call(P=-1) == 1

@@ -272,3 +272,20 @@ def make_qkv(w: Workload, layer: Optional[int] = None, seed_offset: int = 1000):
     if layer is not None:
         return qs[0], ks[0], vs[0]
     return torch.stack(qs), torch.stack(ks), torch.stack(vs)
+
+
+def lm_head_inputs(seed: int, n: int, d_model: int, vocab: int, w_scale: float = 0.02,
+                   integer: bool = False):
+    """Final hidden states H [n][d_model] and LM-head weights W [vocab][d_model],
+    bf16 on the CPU.  H ~ N(0, 1) (a normalised hidden state), W ~ N(0, w_scale^2)
+    (an initialised linear layer); with `integer` both hold small integers in
+    [-2, 2], whose dot products are exact in float32 and tie often."""
+    rng = np.random.default_rng(seed)
+    if integer:
+        h = rng.integers(-2, 3, size=(n, d_model)).astype(np.float32)
+        w = rng.integers(-2, 3, size=(vocab, d_model)).astype(np.float32)
+        return torch.from_numpy(h).to(torch.bfloat16), torch.from_numpy(w).to(torch.bfloat16)
+    h = normal(rng, (n, d_model), "bf16")
+    w = (torch.from_numpy(rng.standard_normal(size=(vocab, d_model), dtype=np.float32)) *
+         w_scale).to(torch.bfloat16)
+    return h, w
