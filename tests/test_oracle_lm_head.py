@@ -1,5 +1,5 @@
 """Pins of the LM-head oracle (oracle/lm_head.py): torch's fp64 matmul and
-argmax, a hand-built case whose winning token and tie are known, and the
+argmax, a hand-built case whose winning tokens and tie are known, and the
 per-node selection."""
 import numpy as np
 import pytest
@@ -8,8 +8,7 @@ import torch
 import oracle
 
 
-@pytest.mark.parametrize("seed", range(3))
-def test_matches_torch(seed):
+def check_matches_torch(seed):
     rng = np.random.default_rng(seed)
     h = rng.standard_normal((7, 96))
     w = rng.standard_normal((500, 96))
@@ -18,9 +17,15 @@ def test_matches_torch(seed):
     assert np.allclose(oracle.lm_head_logits(h, w), h @ w.T)
 
 
-def test_hand_built_winner_and_tie():
-    # node 0's hidden state is e_2; token 5's weight row is 3 e_2, token 9's
-    # is 3 e_2 too (a tie: the lower id wins); every other row is e_2 or less
+@pytest.mark.parametrize("seed", range(3))
+def test_matches_torch(seed):
+    check_matches_torch(seed)
+
+
+def check_hand_built_winner_and_tie():
+    # node 0's hidden state is e_2; the weight rows of tokens 5 and 9 are both
+    # 3 e_2 (a tie: the lower id wins) and every other row is e_2; node 1's
+    # hidden state is -e_0 and only token 11 has a negative first weight
     h = np.zeros((2, 4))
     h[0, 2] = 1.0
     h[1, 0] = -1.0
@@ -29,8 +34,11 @@ def test_hand_built_winner_and_tie():
     w[5, 2] = 3.0
     w[9, 2] = 3.0
     w[11, 0] = -2.0    # node 1: -1 * -2 = 2 beats every other row (0)
-    am = oracle.lm_head_argmax(h, w)
-    assert am.tolist() == [5, 11]
+    assert oracle.lm_head_argmax(h, w).tolist() == [5, 11]
+
+
+def test_hand_built_winner_and_tie():
+    check_hand_built_winner_and_tie()
 
 
 def test_node_subset():

@@ -261,3 +261,39 @@ def test_inversion_at_or_above_is_caught(monkeypatch):
 def test_philox_without_key_schedule_is_caught(monkeypatch):
     monkeypatch.setattr(ts, "_W0", 0)
     assert _some_fail(_sample_pins())
+
+
+# ------------------------------------------------------------ LM head
+
+def _lm_head_pins():
+    from tests import test_oracle_lm_head as lm
+    return [lambda: lm.check_matches_torch(0), lm.check_hand_built_winner_and_tie]
+
+
+def test_lm_head_pins_pass_unmutated():
+    assert not _some_fail(_lm_head_pins())
+
+
+def test_lm_head_highest_id_tie_is_caught(monkeypatch):
+    import oracle
+
+    def last_max(hidden, weight, nodes=None):
+        z = oracle.lm_head_logits(hidden, weight)
+        return (z.shape[1] - 1 - np.argmax(z[:, ::-1], axis=1)).astype(np.int32)
+    monkeypatch.setattr(oracle, "lm_head_argmax", last_max)
+    assert _some_fail(_lm_head_pins())
+
+
+def test_lm_head_dropped_last_feature_is_caught(monkeypatch):
+    import oracle
+    real = oracle.lm_head_logits
+    monkeypatch.setattr(oracle, "lm_head_logits",
+                        lambda h, w: real(np.asarray(h)[:, :-1], np.asarray(w)[:, :-1]))
+    assert _some_fail(_lm_head_pins())
+
+
+def test_lm_head_argmin_is_caught(monkeypatch):
+    import oracle
+    monkeypatch.setattr(oracle, "lm_head_argmax",
+                        lambda h, w, nodes=None: np.argmin(oracle.lm_head_logits(h, w), axis=1))
+    assert _some_fail(_lm_head_pins())
