@@ -297,3 +297,44 @@ def test_lm_head_argmin_is_caught(monkeypatch):
     monkeypatch.setattr(oracle, "lm_head_argmax",
                         lambda h, w, nodes=None: np.argmin(oracle.lm_head_logits(h, w), axis=1))
     assert _some_fail(_lm_head_pins())
+
+
+# ------------------------------------------------------------ losslessness
+
+def _lossless_fails():
+    from tests import test_oracle_lossless as ll
+    try:
+        for plant in (0.7, 1.0):
+            ll.test_speculative_equals_autoregressive(1, 12, plant)
+    except AssertionError:
+        return True
+    return False
+
+
+def test_lossless_pin_passes_unmutated():
+    assert not _lossless_fails()
+
+
+def test_lossless_catches_parent_only_mask(monkeypatch):
+    def two_levels(parent, i):
+        return [i] + ([parent[i]] if parent[i] >= 0 else [])
+    monkeypatch.setattr(tv, "ancestors_inclusive", two_levels)
+    assert _lossless_fails()
+
+
+def test_lossless_catches_compaction_from_the_wrong_row(monkeypatch):
+    real = tv.kv_compact
+
+    def shifted(cache, prefix_len, new_pos):
+        return real(cache, prefix_len + 1, new_pos)
+    monkeypatch.setattr(tv, "kv_compact", shifted)
+    import oracle
+    monkeypatch.setattr(oracle, "kv_compact", shifted)
+    assert _lossless_fails()
+
+
+def test_lossless_catches_a_wrong_bonus_token(monkeypatch):
+    real = tv.accepted_tokens
+    monkeypatch.setattr(tv, "accepted_tokens",
+                        lambda path, am, token: real(path, am, token)[:-1] + [int(token[path[-1]])])
+    assert _lossless_fails()
