@@ -831,6 +831,74 @@ def run_lmhead(args, local_rank):
         "l2": "weights (2.1 GB) larger than L2", "peak_source": peaks["source"]}), flush=True)
 
 
+def run_paged(args, local_rank):
+    """The full step's attention (80 layers, 64/8 heads, d 128, bf16, prefix
+    4096, the 64-node tree) with every layer's cache in a shared page pool
+    (pages shuffled), for page sizes 64, 128 and 256, against the same
+    attention over contiguous caches.  The pool (1.4 GB) exceeds L2.  One
+    JSON line."""
+    import torch
+
+    import speculative_decoding_tree_masked_gb300 as tvp
+    from workloads import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.Stream(dev)
+    w = synth.make_workload(WORKLOAD, seed=args.seed, layers=1)
+    n, layers = w.n, args.layers
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(args.seed)
+    par = torch.from_numpy(w.parent).to(dev)
+    q = torch.randn(layers, n, HQ, D, device=dev, generator=gen).to(torch.bfloat16)
+    out = torch.empty(n, HQ, D, dtype=torch.bfloat16, device=dev)
+    ws = tvp.attn_workspace(n, HQ, HKV, D, torch.bfloat16, PREFIX, dev)
+    reps = max(3, min(args.steps, 20))
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            fn()
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                graph.replay()
+            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ea.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            eb.record(stream)
+        torch.cuda.synchronize()
+        return ea.elapsed_time(eb) * 1e3 / (reps * layers)
+
+    res = {}
+    cap = PREFIX + n
+    kc = torch.randn(layers, HKV, cap, D, device=dev, generator=gen).to(torch.bfloat16)
+    vc = torch.randn_like(kc)
+    res["contiguous"] = timed(lambda: [tvp.tree_attn_verify(q[l], kc[l], vc[l], PREFIX, par,
+                                                            out=out, workspace=ws)
+                                       for l in range(layers)])
+    del kc, vc
+    for ps in (64, 128, 256):
+        t = -(-(PREFIX + n) // ps)
+        pages = t * layers + 8
+        kp = torch.randn(pages, HKV, ps, D, device=dev, generator=gen).to(torch.bfloat16)
+        vp = torch.randn_like(kp)
+        perm = torch.randperm(pages, device=dev, generator=gen).to(torch.int32)
+        tabs = [perm[l * t:(l + 1) * t].contiguous() for l in range(layers)]
+        res[f"page_{ps}"] = timed(lambda: [tvp.tree_attn_verify_paged(
+            q[l], kp, vp, tabs[l], PREFIX, par, out=out, workspace=ws) for l in range(layers)])
+        del kp, vp
+    print(json.dumps({
+        "kernel": "tree attention over paged K/V (tcgen05 kernel + combine)",
+        "workload": f"{layers} layers, {HQ}/{HKV} heads, d {D}, bf16, prefix {PREFIX}, "
+                    f"{n}-node tree; pages shuffled in one pool",
+        "us_per_layer": {k: round(v, 3) for k, v in res.items()},
+        "l2": "caches and pools larger than L2"}), flush=True)
+
+
 def _splits_for(tvp, n, hq, hkv, d, prefix):
     import torch
     nbytes = tvp.attn_workspace_size(n, hq, hkv, d, torch.bfloat16, prefix)
@@ -863,6 +931,8 @@ def main():
                     help="time greedy and sampling acceptance instead of the step")
     ap.add_argument("--expand", action="store_true",
                     help="time the draft side's tree expansion instead of the step")
+    ap.add_argument("--paged", action="store_true",
+                    help="time the attention over paged K/V caches instead of the step")
     ap.add_argument("--lmhead", action="store_true",
                     help="time the LM head fused with the argmax instead of the step")
     ap.add_argument("--sweep", action="store_true",
@@ -877,10 +947,11 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
-    if args.sweep or args.expand or args.sample or args.batch or args.lmhead:
+    if args.sweep or args.expand or args.sample or args.batch or args.lmhead or args.paged:
         if rank == 0:
             mode = (run_sweep if args.sweep else run_expand if args.expand else
-                    run_sample if args.sample else run_lmhead if args.lmhead else run_batch)
+                    run_sample if args.sample else run_lmhead if args.lmhead else
+                    run_paged if args.paged else run_batch)
             mode(args, local_rank)
         return
     if world > 1:

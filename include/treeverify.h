@@ -227,6 +227,62 @@ TV_API tv_status tv_tree_attn_verify_batched(int32_t batch, const void* const* q
                                              int32_t* dev_status, tv_stream_t stream);
 
 /*
+ * Paged K/V caches.  A page pool holds fixed-size pages of key rows,
+ * [num_pages][hkv][page_size][d] (bf16); a request's logical key row r
+ * (rows [0, P) its prefix, row P + j tree node j, as in tv_tree_attn_verify)
+ * is row r % page_size of page page_table[r / page_size].  Many requests
+ * share one pool and each has its own table, so prefixes need no contiguous
+ * room and whole pages can be shared or recycled.  Passage: the same as
+ * tv_tree_attn_verify; paging is the serving form of its cache layout (the
+ * page verifies one request).
+ *
+ * Contract for every paged call:
+ *   page_size     a multiple of 64 (a key block is two 64-row boxes)
+ *   num_pages     >= 1; pools 16-byte aligned
+ *   page_table    device int32 [ceil((P + N) / page_size)]: the pages of rows
+ *                 [0, P + N) in order; an entry outside [0, num_pages) is
+ *                 reported as TV_ERR_INVALID_ARG in dev_status (attention
+ *                 then reads zeros for it; compaction skips the rows)
+ *   rows of those pages past P + N must hold finite values (they are read,
+ *   weighted by exactly zero, so a NaN or an infinity there would leak in)
+ * The attention takes the workspace of tv_attn_workspace_size (the same
+ * plan) and returns TV_ERR_UNSUPPORTED when one CTA's key range spans more
+ * than 1022 pages (very long prefixes with small pages).
+ */
+
+/* tv_tree_attn_verify over a page pool (bf16 only; other arguments as for
+ * tv_tree_attn_verify, less cap). */
+TV_API tv_status tv_tree_attn_verify_paged(const void* q, const void* k_pool, const void* v_pool,
+                                           int32_t num_pages, int32_t page_size,
+                                           const int32_t* page_table, int32_t prefix_len,
+                                           int32_t n_nodes, const int32_t* parent, void* out,
+                                           int32_t hq, int32_t hkv, int32_t d, int32_t dtype,
+                                           float scale, void* workspace, size_t ws_bytes,
+                                           int32_t* dev_status, tv_stream_t stream);
+
+/* tv_tree_attn_verify_batched over one shared page pool: page_table[b] is
+ * request b's table (host array of device pointers); the workspace is that
+ * of tv_attn_batched_workspace_size. */
+TV_API tv_status tv_tree_attn_verify_batched_paged(
+    int32_t batch, const void* const* q, const void* k_pool, const void* v_pool,
+    int32_t num_pages, int32_t page_size, const int32_t* const* page_table,
+    const int32_t* prefix_len, const int32_t* n_nodes, const int32_t* const* parent,
+    void* const* out, int32_t hq, int32_t hkv, int32_t d, int32_t dtype, float scale,
+    void* workspace, size_t ws_bytes, int32_t* dev_status, tv_stream_t stream);
+
+/* tv_kv_compact over page pools: every layer's pool is
+ * [num_pages][hkv][page_size][d] (layer l at l * layer_stride_elems); the
+ * accepted path and the survivors move between logical rows, each mapped
+ * through page_table (the request's table, shared by all layers).  Any
+ * page_size >= 1 is accepted here.  Other arguments as for tv_kv_compact. */
+TV_API tv_status tv_kv_compact_paged(void* k_pool, void* v_pool, int32_t n_layers,
+                                     int64_t layer_stride_elems, int32_t num_pages, int32_t hkv,
+                                     int32_t page_size, int32_t d, int32_t dtype,
+                                     const int32_t* page_table, int32_t prefix_len,
+                                     int32_t n_nodes, const int32_t* new_pos,
+                                     int32_t* dev_status, tv_stream_t stream);
+
+/*
  * tv_tree_accept -- greedy acceptance of the draft tree and the re-root map.
  *
  * Passage: SwiftSpec review page, "What carries the argument" (the tree

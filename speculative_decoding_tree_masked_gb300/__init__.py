@@ -195,6 +195,100 @@ def tree_attn_verify_batched(qs, k_caches, v_caches, prefix_lens, parents, outs=
     return outs
 
 
+def _check_pool(k_pool: torch.Tensor, v_pool: torch.Tensor):
+    if k_pool.dim() != 4 or v_pool.shape != k_pool.shape or v_pool.dtype != k_pool.dtype:
+        raise ValueError("pools must be [num_pages][Hkv][page_size][d] and alike")
+    if not k_pool.is_contiguous() or not v_pool.is_contiguous():
+        raise ValueError("pools must be contiguous")
+    return k_pool.shape
+
+
+def tree_attn_verify_paged(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                           page_table: torch.Tensor, prefix_len: int, parent: torch.Tensor,
+                           out: Optional[torch.Tensor] = None, scale: float = 0.0,
+                           workspace: Optional[torch.Tensor] = None,
+                           status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Tree attention over a paged K/V cache (bf16): pools [num_pages][Hkv]
+    [page_size][d], page_table int32 [ceil((P + N) / page_size)] naming the
+    page of each run of page_size logical rows.  Otherwise as
+    tree_attn_verify."""
+    _need_cuda(q, k_pool, v_pool, page_table, parent)
+    num_pages, hkv, page_size, d = _check_pool(k_pool, v_pool)
+    n, hq, dq = q.shape
+    if dq != d or parent.numel() != n or page_table.dtype != torch.int32:
+        raise ValueError("shape mismatch")
+    if k_pool.dtype != q.dtype or parent.dtype != torch.int32:
+        raise ValueError("dtype mismatch")
+    if page_table.numel() * page_size < prefix_len + n:
+        raise ValueError("page table shorter than prefix + tree")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = attn_workspace(n, hq, hkv, d, q.dtype, prefix_len, q.device)
+    _check(lib().tv_tree_attn_verify_paged(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), num_pages, page_size, _ptr(page_table), prefix_len,
+        n, _ptr(parent), _ptr(out), hq, hkv, d, _dtype_code(q), float(scale), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream, q.device)),
+        "tv_tree_attn_verify_paged")
+    return out
+
+
+def tree_attn_verify_batched_paged(qs, k_pool: torch.Tensor, v_pool: torch.Tensor, page_tables,
+                                   prefix_lens, parents, outs=None, scale: float = 0.0,
+                                   workspace: Optional[torch.Tensor] = None,
+                                   status: Optional[torch.Tensor] = None, stream=None) -> list:
+    """tree_attn_verify_batched over one shared page pool: request b has its
+    own page table page_tables[b] (int32)."""
+    batch = len(qs)
+    if not (len(page_tables) == len(prefix_lens) == len(parents) == batch):
+        raise ValueError("per-request lists differ in length")
+    _need_cuda(k_pool, v_pool, *qs, *page_tables, *parents)
+    num_pages, hkv, page_size, d = _check_pool(k_pool, v_pool)
+    hq = qs[0].shape[1]
+    for q, tab, par, p in zip(qs, page_tables, parents, prefix_lens):
+        if q.shape[1:] != (hq, d) or par.numel() != q.shape[0] or tab.dtype != torch.int32 or \
+                par.dtype != torch.int32 or q.dtype != k_pool.dtype:
+            raise ValueError("shape or dtype mismatch")
+        if tab.numel() * page_size < int(p) + q.shape[0]:
+            raise ValueError("page table shorter than prefix + tree")
+    if outs is None:
+        outs = [torch.empty_like(q) for q in qs]
+    ns = [q.shape[0] for q in qs]
+    if workspace is None:
+        nbytes = attn_batched_workspace_size(ns, hq, hkv, d, qs[0].dtype)
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=qs[0].device)
+    vp = lambda ts: _host_array(ctypes.c_void_p, [_ptr(t) for t in ts])
+    arrs = [vp(qs), vp(page_tables), _host_array(ctypes.c_int32, [int(x) for x in prefix_lens]),
+            _host_array(ctypes.c_int32, ns), vp(parents), vp(outs)]
+    cp = [ctypes.cast(a, ctypes.c_void_p) for a in arrs]
+    _check(lib().tv_tree_attn_verify_batched_paged(
+        batch, cp[0], _ptr(k_pool), _ptr(v_pool), num_pages, page_size, cp[1], cp[2], cp[3],
+        cp[4], cp[5], hq, hkv, d, _dtype_code(qs[0]), float(scale), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(status),
+        _stream(stream, qs[0].device)), "tv_tree_attn_verify_batched_paged")
+    return outs
+
+
+def kv_compact_paged(k_pools: torch.Tensor, v_pools: torch.Tensor, page_table: torch.Tensor,
+                     prefix_len: int, n_nodes: int, new_pos: torch.Tensor,
+                     status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """In-place compaction of paged caches: pools [L][num_pages][Hkv]
+    [page_size][d] (or one layer without L); logical rows map through
+    page_table."""
+    _need_cuda(k_pools, v_pools, page_table, new_pos)
+    if k_pools.shape != v_pools.shape or k_pools.dtype != v_pools.dtype:
+        raise ValueError("k and v pools differ")
+    shape = k_pools.shape if k_pools.dim() == 5 else (1,) + tuple(k_pools.shape)
+    layers, num_pages, hkv, page_size, d = shape
+    if new_pos.dtype != torch.int32 or new_pos.numel() != n_nodes or \
+            page_table.dtype != torch.int32:
+        raise ValueError("new_pos and page_table must be int32")
+    _check(lib().tv_kv_compact_paged(
+        _ptr(k_pools), _ptr(v_pools), layers, num_pages * hkv * page_size * d, num_pages, hkv,
+        page_size, d, _dtype_code(k_pools), _ptr(page_table), prefix_len, n_nodes, _ptr(new_pos),
+        _ptr(status), _stream(stream, k_pools.device)), "tv_kv_compact_paged")
+
+
 def tree_accept(logits: torch.Tensor, token: torch.Tensor, parent: torch.Tensor, prefix_len: int,
                 outs: Optional[dict] = None, status: Optional[torch.Tensor] = None,
                 stream=None) -> dict:

@@ -33,6 +33,15 @@ SIGNATURES = {
     "tv_tree_attn_verify_batched": (c_i32, [c_i32, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr,
                                             c_ptr, c_ptr, c_i32, c_i32, c_i32, c_i32,
                                             ctypes.c_float, c_ptr, c_size, c_ptr, c_ptr]),
+    "tv_tree_attn_verify_paged": (c_i32, [c_ptr, c_ptr, c_ptr, c_i32, c_i32, c_ptr, c_i32, c_i32,
+                                          c_ptr, c_ptr, c_i32, c_i32, c_i32, c_i32,
+                                          ctypes.c_float, c_ptr, c_size, c_ptr, c_ptr]),
+    "tv_tree_attn_verify_batched_paged": (c_i32, [c_i32, c_ptr, c_ptr, c_ptr, c_i32, c_i32, c_ptr,
+                                                  c_ptr, c_ptr, c_ptr, c_ptr, c_i32, c_i32, c_i32,
+                                                  c_i32, ctypes.c_float, c_ptr, c_size, c_ptr,
+                                                  c_ptr]),
+    "tv_kv_compact_paged": (c_i32, [c_ptr, c_ptr, c_i32, c_i64, c_i32, c_i32, c_i32, c_i32, c_i32,
+                                    c_ptr, c_i32, c_i32, c_ptr, c_ptr, c_ptr]),
     "tv_tree_accept": (c_i32, [c_ptr, c_i32, c_ptr, c_ptr, c_i32, c_i32, c_ptr, c_ptr, c_ptr,
                                c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr]),
     "tv_kv_compact": (c_i32, [c_ptr, c_ptr, c_i32, c_i64, c_i32, c_i64, c_i32, c_i32, c_i32,

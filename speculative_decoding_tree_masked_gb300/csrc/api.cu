@@ -30,6 +30,49 @@ tv_status check_attn_shape(int32_t n, int32_t hq, int32_t hkv, int32_t d, int32_
   return TV_OK;
 }
 
+// Page pools [num_pages][hkv][page_size][d] of bf16: pages of whole 64-row
+// boxes, coordinates within int32.
+tv_status check_paging(int32_t num_pages, int32_t page_size, int32_t hkv, int32_t d) {
+  if (num_pages < 1 || page_size < 64 || page_size % 64 != 0) return TV_ERR_INVALID_ARG;
+  if ((int64_t)num_pages * hkv * page_size * d > ((int64_t)1 << 40)) return TV_ERR_UNSUPPORTED;
+  return TV_OK;
+}
+
+tv::AttnProblem attn_problem(const void* q, const void* k, const void* v, int64_t cap,
+                             int32_t prefix_len, int32_t n_nodes, const int32_t* parent,
+                             void* out, int32_t hq, int32_t hkv, int32_t d, int32_t dtype,
+                             float scale, int32_t* dev_status) {
+  tv::AttnProblem p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.parent = parent;
+  p.dev_status = dev_status;
+  p.cap = cap;
+  p.prefix = prefix_len;
+  p.n = n_nodes;
+  p.hq = hq;
+  p.hkv = hkv;
+  p.d = d;
+  p.dtype = dtype;
+  const float sc = scale > 0.f ? scale : 1.0f / std::sqrt((float)d);
+  p.scale_log2 = sc * 1.4426950408889634f;  // log2(e)
+  return p;
+}
+
+// The attention kernel, then the merge of its split partials.
+tv_status run_attention(const tv::AttnProblem& p, const tv::SplitPlan& plan, void* workspace,
+                        tv_stream_t stream) {
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  float* ws = static_cast<float*>(workspace);
+  const bool tc = tv::use_tensor_cores(p.dtype);
+  cudaError_t e = tc ? tv::launch_attn_tc(p, plan, ws, s) : tv::launch_attn_simt(p, plan, ws, s);
+  if (e != cudaSuccess) return TV_ERR_CUDA;
+  if (tc && plan.splits == 1) return TV_OK;  // the kernel wrote the normalised output
+  return from_cuda(tv::launch_combine(p, plan, ws, s));
+}
+
 }  // namespace
 
 extern "C" {
@@ -89,30 +132,42 @@ tv_status tv_tree_attn_verify(const void* q, const void* k_cache, const void* v_
   const tv::SplitPlan plan = tv::plan_attention(n_nodes, hq, hkv, d, dtype, prefix_len, sms);
   if (ws_bytes < plan.ws_bytes) return TV_ERR_CAPACITY;
 
-  tv::AttnProblem p{};
-  p.q = q;
-  p.k = k_cache;
-  p.v = v_cache;
-  p.out = out;
-  p.parent = parent;
-  p.dev_status = dev_status;
-  p.cap = cap;
-  p.prefix = prefix_len;
-  p.n = n_nodes;
-  p.hq = hq;
-  p.hkv = hkv;
-  p.d = d;
-  p.dtype = dtype;
-  const float sc = scale > 0.f ? scale : 1.0f / std::sqrt((float)d);
-  p.scale_log2 = sc * 1.4426950408889634f;  // log2(e)
+  const tv::AttnProblem p = attn_problem(q, k_cache, v_cache, cap, prefix_len, n_nodes, parent,
+                                         out, hq, hkv, d, dtype, scale, dev_status);
 
-  auto s = reinterpret_cast<cudaStream_t>(stream);
-  float* ws = static_cast<float*>(workspace);
-  const bool tc = tv::use_tensor_cores(dtype);
-  cudaError_t e = tc ? tv::launch_attn_tc(p, plan, ws, s) : tv::launch_attn_simt(p, plan, ws, s);
-  if (e != cudaSuccess) return TV_ERR_CUDA;
-  if (tc && plan.splits == 1) return TV_OK;  // the kernel wrote the normalised output
-  return from_cuda(tv::launch_combine(p, plan, ws, s));
+  return run_attention(p, plan, workspace, stream);
+}
+
+tv_status tv_tree_attn_verify_paged(const void* q, const void* k_pool, const void* v_pool,
+                                    int32_t num_pages, int32_t page_size,
+                                    const int32_t* page_table, int32_t prefix_len,
+                                    int32_t n_nodes, const int32_t* parent, void* out, int32_t hq,
+                                    int32_t hkv, int32_t d, int32_t dtype, float scale,
+                                    void* workspace, size_t ws_bytes, int32_t* dev_status,
+                                    tv_stream_t stream) {
+  tv_status st = check_attn_shape(n_nodes, hq, hkv, d, dtype);
+  if (st != TV_OK) return st;
+  if (!q || !k_pool || !v_pool || !page_table || !parent || !out || !workspace)
+    return TV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
+      !aligned16(workspace))
+    return TV_ERR_INVALID_ARG;
+  if (prefix_len < 0 || !(scale >= 0.f) || std::isinf(scale)) return TV_ERR_INVALID_ARG;
+  st = check_paging(num_pages, page_size, hkv, d);
+  if (st != TV_OK) return st;
+  if (dtype != TV_BF16) return TV_ERR_UNSUPPORTED;
+  if ((int64_t)prefix_len + n_nodes > INT32_MAX / 2) return TV_ERR_UNSUPPORTED;
+  const int sms = tv::device_sm_count();
+  if (sms <= 0) return TV_ERR_CUDA;
+  const tv::SplitPlan plan = tv::plan_attention(n_nodes, hq, hkv, d, dtype, prefix_len, sms);
+  if (ws_bytes < plan.ws_bytes) return TV_ERR_CAPACITY;
+  if (plan.keys_per_split / page_size + 2 > tv::kMaxPageSlots) return TV_ERR_UNSUPPORTED;
+  tv::AttnProblem p = attn_problem(q, k_pool, v_pool, 0, prefix_len, n_nodes, parent, out, hq, hkv,
+                                   d, dtype, scale, dev_status);
+  p.page_table = page_table;
+  p.page_size = page_size;
+  p.num_pages = num_pages;
+  return run_attention(p, plan, workspace, stream);
 }
 
 size_t tv_attn_batched_workspace_size(int32_t batch, const int32_t* n_nodes, int32_t hq,
@@ -189,6 +244,78 @@ tv_status tv_tree_attn_verify_batched(int32_t batch, const void* const* q,
       if (st != TV_OK) return st;
     }
   return TV_OK;
+}
+
+tv_status tv_tree_attn_verify_batched_paged(
+    int32_t batch, const void* const* q, const void* k_pool, const void* v_pool,
+    int32_t num_pages, int32_t page_size, const int32_t* const* page_table,
+    const int32_t* prefix_len, const int32_t* n_nodes, const int32_t* const* parent,
+    void* const* out, int32_t hq, int32_t hkv, int32_t d, int32_t dtype, float scale,
+    void* workspace, size_t ws_bytes, int32_t* dev_status, tv_stream_t stream) {
+  if (batch < 1 || batch > TV_MAX_BATCH) return TV_ERR_INVALID_ARG;
+  if (!q || !k_pool || !v_pool || !page_table || !prefix_len || !n_nodes || !parent || !out ||
+      !workspace)
+    return TV_ERR_INVALID_ARG;
+  if (!aligned16(workspace) || !aligned16(k_pool) || !aligned16(v_pool)) return TV_ERR_INVALID_ARG;
+  if (!(scale >= 0.f) || std::isinf(scale)) return TV_ERR_INVALID_ARG;
+  tv_status st = check_paging(num_pages, page_size, hkv, d);
+  if (st != TV_OK) return st;
+  for (int b = 0; b < batch; ++b) {
+    st = check_attn_shape(n_nodes[b], hq, hkv, d, dtype);
+    if (st != TV_OK) return st;
+    if (!q[b] || !page_table[b] || !parent[b] || !out[b]) return TV_ERR_INVALID_ARG;
+    if (!aligned16(q[b]) || !aligned16(out[b])) return TV_ERR_INVALID_ARG;
+    if (prefix_len[b] < 0) return TV_ERR_INVALID_ARG;
+    if ((int64_t)prefix_len[b] + n_nodes[b] > INT32_MAX / 2) return TV_ERR_UNSUPPORTED;
+  }
+  if (dtype != TV_BF16) return TV_ERR_UNSUPPORTED;
+  const int sms = tv::device_sm_count();
+  if (sms <= 0) return TV_ERR_CUDA;
+  tv::SplitPlan plans[TV_MAX_BATCH];
+  size_t offs[TV_MAX_BATCH], total = 0;
+  tv::plan_attention_batched(batch, n_nodes, prefix_len, hq, hkv, d, sms, plans, offs, &total);
+  if (ws_bytes < total) return TV_ERR_CAPACITY;
+  tv::AttnProblem probs[TV_MAX_BATCH];
+  float* ws[TV_MAX_BATCH];
+  for (int b = 0; b < batch; ++b) {
+    if (plans[b].keys_per_split / page_size + 2 > tv::kMaxPageSlots) return TV_ERR_UNSUPPORTED;
+    probs[b] = attn_problem(q[b], k_pool, v_pool, 0, prefix_len[b], n_nodes[b], parent[b], out[b],
+                            hq, hkv, d, dtype, scale, dev_status);
+    probs[b].page_table = page_table[b];
+    probs[b].page_size = page_size;
+    probs[b].num_pages = num_pages;
+    ws[b] = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + offs[b]);
+  }
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  if (tv::launch_attn_tc_batched(probs, plans, batch, ws, s) != cudaSuccess) return TV_ERR_CUDA;
+  for (int b = 0; b < batch; ++b)
+    if (plans[b].splits > 1) {
+      st = from_cuda(tv::launch_combine(probs[b], plans[b], ws[b], s));
+      if (st != TV_OK) return st;
+    }
+  return TV_OK;
+}
+
+tv_status tv_kv_compact_paged(void* k_pool, void* v_pool, int32_t n_layers,
+                              int64_t layer_stride_elems, int32_t num_pages, int32_t hkv,
+                              int32_t page_size, int32_t d, int32_t dtype,
+                              const int32_t* page_table, int32_t prefix_len, int32_t n_nodes,
+                              const int32_t* new_pos, int32_t* dev_status, tv_stream_t stream) {
+  const int es = elem_size(dtype);
+  if (!k_pool || !v_pool || !page_table || !new_pos || es == 0) return TV_ERR_INVALID_ARG;
+  if (n_layers < 1 || hkv < 1 || d < 1 || prefix_len < 0) return TV_ERR_INVALID_ARG;
+  if (num_pages < 1 || page_size < 1) return TV_ERR_INVALID_ARG;
+  if (n_nodes < 1 || n_nodes > TV_MAX_NODES) return TV_ERR_INVALID_ARG;
+  const int64_t row_bytes = (int64_t)d * es;
+  if (row_bytes % 16 != 0 || row_bytes > 512) return TV_ERR_UNSUPPORTED;
+  if (!aligned16(k_pool) || !aligned16(v_pool)) return TV_ERR_INVALID_ARG;
+  if (layer_stride_elems < (int64_t)num_pages * hkv * page_size * d) return TV_ERR_INVALID_ARG;
+  if ((int64_t)n_layers * hkv * 2 > INT32_MAX) return TV_ERR_UNSUPPORTED;
+  if ((int64_t)prefix_len + n_nodes > INT32_MAX / 2) return TV_ERR_UNSUPPORTED;
+  return from_cuda(tv::launch_compact(k_pool, v_pool, n_layers, layer_stride_elems * es, hkv,
+                                      page_size, (int32_t)row_bytes, prefix_len, n_nodes, new_pos,
+                                      dev_status, reinterpret_cast<cudaStream_t>(stream),
+                                      page_table, page_size, num_pages));
 }
 
 tv_status tv_tree_accept(const float* logits, int32_t vocab, const int32_t* token,

@@ -87,6 +87,7 @@ constexpr int kStages = 2;       // K/V ring depth
 constexpr int kThreads = 320;
 constexpr int kSoftmaxWarp0 = 2;
 constexpr int kWarpsPerTile = 4;  // softmax warps of one row tile
+constexpr int kPageRows = 64;     // rows of one paged K/V box (half a key block)
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr long long kWaitCycles = 4000000000LL;
@@ -101,6 +102,10 @@ struct TcParams {
   int32_t n, hq, hkv, prefix, keys, keys_per_split, splits, rows_per_head;
   int32_t q_tma;  // 1: Q tiles arrive by TMA (G divides 128), 0: threads gather them
   float scale_log2;
+  // paged K/V (null: one contiguous cache per KV head): logical key row r
+  // is row r % page_size of page page_table[r / page_size] of the pool
+  const int32_t* page_table;
+  int32_t page_size, num_pages;
 };
 
 // Kernel argument: up to MAXB requests, each with its tensor maps (K, V, Q,
@@ -120,7 +125,7 @@ struct TcBatch {
   uint32_t cta[MAXB == 1 ? 1 : kMaxBatchCtas];
 };
 
-template <int D>
+template <int D, bool PAGED>
 struct Layout {
   static constexpr uint32_t kQTile = kBM * D * 2;   // bytes of one Q tile
   static constexpr uint32_t kKV = kBN * D * 2;      // bytes of one K (or V) block
@@ -128,7 +133,8 @@ struct Layout {
   static constexpr uint32_t kK = kQ + kTiles * kQTile;
   static constexpr uint32_t kV = kK + kStages * kKV;
   static constexpr uint32_t kPar = kV + kStages * kKV;
-  static constexpr uint32_t kBar = kPar + kMaxNodes * 4;
+  static constexpr uint32_t kPtab = kPar + kMaxNodes * 4;   // the CTA's page-table slice
+  static constexpr uint32_t kBar = kPtab + (PAGED ? kMaxPageSlots * 4 : 0);
   static constexpr uint32_t kNumBars = 3 * kTiles + 4 * kStages + kTiles + 2;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kMisc + 16;
@@ -207,10 +213,10 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int D, int MAXB>
+template <int D, int MAXB, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
-  using L = Layout<D>;
+  using L = Layout<D, PAGED>;
   int b = 0, split, g, rgroup;
   if (MAXB == 1) {
     split = blockIdx.x;
@@ -270,23 +276,52 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
+  // Paged K/V: a key block is two 64-row boxes, each from its own page.  A
+  // box past the last key is moved back onto the last 64-row piece that
+  // holds keys (its keys are hidden either way), so every page looked up is
+  // one the table maps.  The CTA's slice of the table is staged in shared
+  // memory; the first block, requested before that, reads the table itself.
+  constexpr bool paged = PAGED;
+  constexpr int kHalves = kBN / kPageRows;
+  const int last64 = ((p.keys - 1) / kPageRows) * kPageRows;
+  const int pfirst = paged ? kbeg / p.page_size : 0;
+  int32_t* ptab = reinterpret_cast<int32_t*>(sm + L::kPtab);
+  auto load_block = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar, int j,
+                        bool table_in_global) {
+    if (!paged) {
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        ptx::tma_load_3d(dst + c * (kBN * 128), map, bar, c * 64, kbeg + j * kBN, g);
+      return;
+    }
+    // both pages are looked up before either copy is issued, so that the
+    // table reads overlap
+    int page[kHalves], off[kHalves];
+#pragma unroll
+    for (int h = 0; h < kHalves; ++h) {
+      const int row = min(kbeg + j * kBN + h * kPageRows, last64);
+      const int slot = row / p.page_size;
+      page[h] = table_in_global ? __ldg(p.page_table + slot) : ptab[slot - pfirst];
+      off[h] = row - slot * p.page_size;
+    }
+#pragma unroll
+    for (int h = 0; h < kHalves; ++h)
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        ptx::tma_load_4d(dst + c * (kBN * 128) + h * (kPageRows * 128), map, bar, c * 64, off[h],
+                         g, page[h]);
+  };
   // The producer thread (tid 0) starts streaming K/V at once: the first
   // kStages blocks need no free slot and do not depend on Q.
   auto load_k = [&](int j) {
     const int s = j % kStages;
     ptx::mbar_arrive_expect_tx(bars.k_full(s), L::kKV);
-#pragma unroll
-    for (int c = 0; c < D / 64; ++c)
-      ptx::tma_load_3d(base + L::kK + s * L::kKV + c * (kBN * 128), kmap, bars.k_full(s), c * 64,
-                       kbeg + j * kBN, g);
+    load_block(kmap, base + L::kK + s * L::kKV, bars.k_full(s), j, j == 0);
   };
   auto load_v = [&](int j) {
     const int s = j % kStages;
     ptx::mbar_arrive_expect_tx(bars.v_full(s), L::kKV);
-#pragma unroll
-    for (int c = 0; c < D / 64; ++c)
-      ptx::tma_load_3d(base + L::kV + s * L::kKV + c * (kBN * 128), vmap, bars.v_full(s), c * 64,
-                       kbeg + j * kBN, g);
+    load_block(vmap, base + L::kV + s * L::kKV, bars.v_full(s), j, false);
   };
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
@@ -305,6 +340,15 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
   }
   if (tid == 0 && nb > 0) load_k(0);  // V_0 follows once K_0 has landed
   for (int i = tid; i < p.n; i += kThreads) par[i] = p.parent[i];
+  if (PAGED && nb > 0) {
+    // the pages of rows [kbeg, the last row a box of this CTA starts at]
+    const int plast = min(kbeg + (nb - 1) * kBN + kPageRows, last64) / p.page_size;
+    for (int i = tid; i <= plast - pfirst; i += kThreads) {
+      const int page = p.page_table[pfirst + i];
+      if (page < 0 || page >= p.num_pages) report(p.dev_status, TV_ERR_INVALID_ARG);
+      ptab[i] = page;
+    }
+  }
   if (!p.q_tma) {
     // Q tiles into shared memory in the K-major 128-byte-swizzled layout:
     // 64-element column chunks of [128 rows][128 B], the 16-byte piece c of
@@ -745,6 +789,23 @@ bool make_kv_map(CUtensorMap* map, const void* base, int d, int rows, int64_t ca
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D map over a page pool [pages][hkv][page_size][d] (bf16): boxes of 64
+// columns x 64 rows of one page and KV head, 128-byte swizzle.
+bool make_paged_kv_map(CUtensorMap* map, const void* base, int d, int page_size, int hkv,
+                       int num_pages) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)page_size, (cuuint64_t)hkv,
+                              (cuuint64_t)num_pages};
+  const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)page_size * d * 2,
+                                 (cuuint64_t)hkv * page_size * d * 2};
+  const cuuint32_t box[4] = {64, (cuuint32_t)kPageRows, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D map over Q [n][hq][d] (bf16): boxes of 64 columns x G heads x 128/G
 // nodes (one 128-row tile of a KV head's query group), 128-byte swizzle,
 // nodes past the tree read as zero.
@@ -777,15 +838,16 @@ bool make_q_map(CUtensorMap* map, const void* base, int d, int n, int hq, int gr
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int MAXB>
+template <int D, int MAXB, bool PAGED>
 cudaError_t set_smem_attr() {
   static bool attr_set[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(attn_tc_kernel<D, MAXB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)Layout<D>::kAlloc);
+    e = cudaFuncSetAttribute(attn_tc_kernel<D, MAXB, PAGED>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Layout<D, PAGED>::kAlloc);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
@@ -797,9 +859,14 @@ template <int D>
 bool fill_request(const AttnProblem& p, const SplitPlan& plan, float* ws, CUtensorMap* kmap,
                   CUtensorMap* vmap, CUtensorMap* qmap, CUtensorMap* omap, TcParams* tp) {
   const int rows = p.prefix + p.n;
-  if (!make_kv_map(kmap, p.k, D, rows, p.cap, p.hkv) ||
-      !make_kv_map(vmap, p.v, D, rows, p.cap, p.hkv))
+  if (p.page_table != nullptr) {
+    if (!make_paged_kv_map(kmap, p.k, D, p.page_size, p.hkv, p.num_pages) ||
+        !make_paged_kv_map(vmap, p.v, D, p.page_size, p.hkv, p.num_pages))
+      return false;
+  } else if (!make_kv_map(kmap, p.k, D, rows, p.cap, p.hkv) ||
+             !make_kv_map(vmap, p.v, D, rows, p.cap, p.hkv)) {
     return false;
+  }
   const int group = p.hq / p.hkv;
   const bool q_tma = (kBM % group) == 0;
   if (q_tma && !make_q_map(qmap, p.q, D, p.n, p.hq, group)) return false;
@@ -830,12 +897,15 @@ bool fill_request(const AttnProblem& p, const SplitPlan& plan, float* ws, CUtens
   tp->rows_per_head = (p.hq / p.hkv) * p.n;
   tp->scale_log2 = p.scale_log2;
   tp->q_tma = q_tma ? 1 : 0;
+  tp->page_table = p.page_table;
+  tp->page_size = p.page_size;
+  tp->num_pages = p.num_pages;
   return true;
 }
 
-template <int D>
+template <int D, bool PAGED>
 cudaError_t launch_d(const AttnProblem& p, const SplitPlan& plan, float* ws, cudaStream_t s) {
-  cudaError_t e = set_smem_attr<D, 1>();
+  cudaError_t e = set_smem_attr<D, 1, PAGED>();
   if (e != cudaSuccess) return e;
   TcBatch<1> batch;
   memset(&batch, 0, sizeof(batch));
@@ -843,14 +913,14 @@ cudaError_t launch_d(const AttnProblem& p, const SplitPlan& plan, float* ws, cud
                        &batch.omap[0], &batch.req[0]))
     return cudaErrorInvalidValue;
   const dim3 grid(plan.splits, plan.row_tiles, p.hkv);
-  attn_tc_kernel<D, 1><<<grid, kThreads, Layout<D>::kAlloc, s>>>(batch);
+  attn_tc_kernel<D, 1, PAGED><<<grid, kThreads, Layout<D, PAGED>::kAlloc, s>>>(batch);
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool PAGED>
 cudaError_t launch_batched_d(const AttnProblem* probs, const SplitPlan* plans, int batch_n,
                              float* const* ws, cudaStream_t s) {
-  cudaError_t e = set_smem_attr<D, kMaxBatch>();
+  cudaError_t e = set_smem_attr<D, kMaxBatch, PAGED>();
   if (e != cudaSuccess) return e;
   // about 13 KB: built on the heap, passed by value to the launch
   auto* batch = new TcBatch<kMaxBatch>;
@@ -858,7 +928,8 @@ cudaError_t launch_batched_d(const AttnProblem* probs, const SplitPlan* plans, i
   int ctas = 0;
   bool ok = batch_n <= kMaxBatch;
   for (int b = 0; ok && b < batch_n; ++b) {
-    ok = fill_request<D>(probs[b], plans[b], ws[b], &batch->kmap[b], &batch->vmap[b],
+    ok = (probs[b].page_table != nullptr) == PAGED;  // one launch is all paged or none
+    ok = ok && fill_request<D>(probs[b], plans[b], ws[b], &batch->kmap[b], &batch->vmap[b],
                          &batch->qmap[b], &batch->omap[b], &batch->req[b]);
     for (int g = 0; ok && g < probs[b].hkv; ++g)
       for (int rg = 0; ok && rg < plans[b].row_tiles; ++rg)
@@ -867,7 +938,8 @@ cudaError_t launch_batched_d(const AttnProblem* probs, const SplitPlan* plans, i
           if (ok) batch->cta[ctas++] = pack_cta(b, g, rg, sp);
         }
   }
-  if (ok) attn_tc_kernel<D, kMaxBatch><<<ctas, kThreads, Layout<D>::kAlloc, s>>>(*batch);
+  if (ok)
+    attn_tc_kernel<D, kMaxBatch, PAGED><<<ctas, kThreads, Layout<D, PAGED>::kAlloc, s>>>(*batch);
   delete batch;
   if (!ok) return cudaErrorInvalidValue;
   return cudaGetLastError();
@@ -877,14 +949,19 @@ cudaError_t launch_batched_d(const AttnProblem* probs, const SplitPlan* plans, i
 
 cudaError_t launch_attn_tc(const AttnProblem& p, const SplitPlan& plan, float* ws,
                            cudaStream_t s) {
-  return p.d == 128 ? launch_d<128>(p, plan, ws, s) : launch_d<64>(p, plan, ws, s);
+  if (p.page_table != nullptr)
+    return p.d == 128 ? launch_d<128, true>(p, plan, ws, s) : launch_d<64, true>(p, plan, ws, s);
+  return p.d == 128 ? launch_d<128, false>(p, plan, ws, s) : launch_d<64, false>(p, plan, ws, s);
 }
 
 cudaError_t launch_attn_tc_batched(const AttnProblem* probs, const SplitPlan* plans,
                                    int batch_n, float* const* ws, cudaStream_t s) {
   if (batch_n < 1) return cudaErrorInvalidValue;
-  return probs[0].d == 128 ? launch_batched_d<128>(probs, plans, batch_n, ws, s)
-                           : launch_batched_d<64>(probs, plans, batch_n, ws, s);
+  if (probs[0].page_table != nullptr)
+    return probs[0].d == 128 ? launch_batched_d<128, true>(probs, plans, batch_n, ws, s)
+                             : launch_batched_d<64, true>(probs, plans, batch_n, ws, s);
+  return probs[0].d == 128 ? launch_batched_d<128, false>(probs, plans, batch_n, ws, s)
+                           : launch_batched_d<64, false>(probs, plans, batch_n, ws, s);
 }
 
 }  // namespace tv

@@ -6,6 +6,10 @@
 // synchronises, and the rows are written to their destinations.  Reading all
 // sources before writing any destination makes the in-place gather safe even
 // though destinations overlap sources.  Rows move as 16-byte vectors.
+//
+// A paged cache (a pool [pages][hkv][page_size][d] per layer) maps logical
+// row r to row r % page_size of page page_table[r / page_size]; a move whose
+// source or destination page is outside the pool is skipped and reported.
 #include "common.cuh"
 #include "internal.h"
 
@@ -18,7 +22,8 @@ constexpr int kCompactThreads = 256;
 __global__ void __launch_bounds__(kCompactThreads)
 compact_kernel(char* __restrict__ kc, char* __restrict__ vc, int hkv, long long layer_stride,
                long long cap, int row_bytes, int prefix, int n,
-               const int32_t* __restrict__ new_pos, int32_t* dev_status) {
+               const int32_t* __restrict__ new_pos, const int32_t* __restrict__ page_table,
+               int page_size, int num_pages, int32_t* dev_status) {
   extern __shared__ uint4 buf[];
   __shared__ int src_row[kMaxNodes], dst_row[kMaxNodes];
   __shared__ uint32_t used[kMaskWords];
@@ -28,7 +33,15 @@ compact_kernel(char* __restrict__ kc, char* __restrict__ vc, int hkv, long long 
   const int which = slab & 1;
   const int g = (slab >> 1) % hkv;
   const int layer = (slab >> 1) / hkv;
-  char* base = (which ? vc : kc) + (size_t)layer * layer_stride + (size_t)g * cap * row_bytes;
+  char* lbase = (which ? vc : kc) + (size_t)layer * layer_stride;
+  char* base = lbase + (size_t)g * cap * row_bytes;
+  // byte offset of logical row r, or -1 when its page is outside the pool
+  auto row_at = [&](int r) -> long long {
+    if (page_table == nullptr) return (long long)(base - lbase) + (long long)r * row_bytes;
+    const int page = __ldg(page_table + r / page_size);
+    if (page < 0 || page >= num_pages) return -1;
+    return (((long long)page * hkv + g) * page_size + r % page_size) * row_bytes;
+  };
 
   if (tid == 0) count = 0;
   if (tid < kMaskWords) used[tid] = 0u;
@@ -46,9 +59,13 @@ compact_kernel(char* __restrict__ kc, char* __restrict__ vc, int hkv, long long 
       if (!in_range || !fresh) {
         if (slab == 0) report(dev_status, TV_ERR_INVALID_ARG);
       } else if (pos != prefix + tid) {
-        const int k = atomicAdd(&count, 1);
-        src_row[k] = prefix + tid;
-        dst_row[k] = pos;
+        if (row_at(prefix + tid) < 0 || row_at(pos) < 0) {
+          if (slab == 0) report(dev_status, TV_ERR_INVALID_ARG);
+        } else {
+          const int k = atomicAdd(&count, 1);
+          src_row[k] = prefix + tid;
+          dst_row[k] = pos;
+        }
       }
     }
   }
@@ -57,12 +74,12 @@ compact_kernel(char* __restrict__ kc, char* __restrict__ vc, int hkv, long long 
   const int chunks = row_bytes >> 4;
   for (int e = tid; e < moves * chunks; e += kCompactThreads) {
     const int r = e / chunks, c = e - r * chunks;
-    buf[e] = reinterpret_cast<const uint4*>(base + (size_t)src_row[r] * row_bytes)[c];
+    buf[e] = reinterpret_cast<const uint4*>(lbase + row_at(src_row[r]))[c];
   }
   __syncthreads();
   for (int e = tid; e < moves * chunks; e += kCompactThreads) {
     const int r = e / chunks, c = e - r * chunks;
-    reinterpret_cast<uint4*>(base + (size_t)dst_row[r] * row_bytes)[c] = buf[e];
+    reinterpret_cast<uint4*>(lbase + row_at(dst_row[r]))[c] = buf[e];
   }
 }
 
@@ -90,7 +107,8 @@ tree_mask_kernel(const int32_t* __restrict__ parent, int n, uint32_t* __restrict
 cudaError_t launch_compact(void* k, void* v, int32_t layers, int64_t layer_stride_bytes,
                            int32_t hkv, int64_t cap, int32_t row_bytes, int32_t prefix,
                            int32_t n, const int32_t* new_pos, int32_t* dev_status,
-                           cudaStream_t s) {
+                           cudaStream_t s, const int32_t* page_table, int32_t page_size,
+                           int32_t num_pages) {
   const size_t smem = (size_t)n * row_bytes;
   static bool attr_set[64];  // per device
   int dev = 0;
@@ -105,7 +123,7 @@ cudaError_t launch_compact(void* k, void* v, int32_t layers, int64_t layer_strid
   const unsigned grid = (unsigned)layers * (unsigned)hkv * 2u;
   compact_kernel<<<grid, kCompactThreads, smem, s>>>(
       static_cast<char*>(k), static_cast<char*>(v), hkv, layer_stride_bytes, cap, row_bytes,
-      prefix, n, new_pos, dev_status);
+      prefix, n, new_pos, page_table, page_size, num_pages, dev_status);
   return cudaGetLastError();
 }
 

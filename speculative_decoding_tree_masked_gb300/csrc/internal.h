@@ -29,7 +29,16 @@ struct AttnProblem {
   int32_t d;
   int32_t dtype;
   float scale_log2;  // softmax scale * log2(e)
+  // paged K/V (bf16 only): k and v are page pools [num_pages][hkv][page_size][d]
+  // and logical key row r lives in page page_table[r / page_size]; null for
+  // contiguous caches [hkv][cap][d]
+  const int32_t* page_table = nullptr;
+  int32_t page_size = 0;
+  int32_t num_pages = 0;
 };
+
+// Most page-table entries one CTA of the tensor-core kernel stages.
+constexpr int kMaxPageSlots = 1024;
 
 // Split-KV plan: key range [0, P + N) cut into `splits` chunks of
 // `keys_per_split` keys (a multiple of the kernel's key block).
@@ -111,10 +120,13 @@ cudaError_t launch_accept_sampled(const float* logits, int32_t vocab, const int3
                                   int32_t* sampled, int32_t* m, int32_t* path,
                                   int32_t* out_tokens, int32_t* new_pos, int32_t* new_parent,
                                   int32_t* n_survivors, int32_t* dev_status, cudaStream_t s);
+// Contiguous caches [hkv][cap][row] per layer, or (page_table given) page
+// pools [num_pages][hkv][page_size][row] per layer.
 cudaError_t launch_compact(void* k, void* v, int32_t layers, int64_t layer_stride_bytes,
                            int32_t hkv, int64_t cap, int32_t row_bytes, int32_t prefix,
                            int32_t n, const int32_t* new_pos, int32_t* dev_status,
-                           cudaStream_t s);
+                           cudaStream_t s, const int32_t* page_table = nullptr,
+                           int32_t page_size = 0, int32_t num_pages = 0);
 
 // The target's LM head fused with the argmax (bf16 hidden states and weights).
 size_t lm_head_workspace_bytes(int32_t n, int32_t vocab, int sm_count);

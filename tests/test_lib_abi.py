@@ -206,3 +206,38 @@ def test_accept_tokens_host_checks(lib):
     assert call(n=0) == 1
     assert call(n=129) == 1
     assert call(P=-1) == 1
+
+
+def test_paged_host_checks(lib):
+    import ctypes
+    fake = ctypes.c_void_p(0x1000)
+
+    def attn(**kw):
+        a = dict(q=fake, kp=fake, vp=fake, pages=10, ps=64, tab=fake, P=100, n=8, hq=8, hkv=2,
+                 d=128, dt=1, ws=fake, wsb=1 << 30)
+        a.update(kw)
+        return lib.tv_tree_attn_verify_paged(a["q"], a["kp"], a["vp"], a["pages"], a["ps"],
+                                             a["tab"], a["P"], a["n"], fake, fake, a["hq"],
+                                             a["hkv"], a["d"], a["dt"], 0.0, a["ws"], a["wsb"],
+                                             None, None)
+    assert attn(tab=None) == 1
+    assert attn(ps=48) == 1                     # not a multiple of 64
+    assert attn(ps=0) == 1
+    assert attn(pages=0) == 1
+    assert attn(kp=ctypes.c_void_p(0x1008)) == 1
+    assert attn(d=96) == 2
+    assert attn(dt=0) == 2                      # paged attention is bf16 only
+    assert attn(n=129) == 1
+
+    def compact(**kw):
+        a = dict(kp=fake, vp=fake, L=2, stride=10 * 2 * 64 * 128, pages=10, hkv=2, ps=64, d=128,
+                 dt=1, tab=fake, P=100, n=8)
+        a.update(kw)
+        return lib.tv_kv_compact_paged(a["kp"], a["vp"], a["L"], a["stride"], a["pages"],
+                                       a["hkv"], a["ps"], a["d"], a["dt"], a["tab"], a["P"],
+                                       a["n"], fake, None, None)
+    assert compact(tab=None) == 1
+    assert compact(stride=100) == 1             # layers would overlap
+    assert compact(n=0) == 1
+    assert compact(d=12) == 2                   # rows not whole 16-byte vectors
+    assert compact(pages=0) == 1
