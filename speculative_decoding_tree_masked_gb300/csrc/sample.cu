@@ -8,13 +8,17 @@
 // stays lossless.
 //
 // One 8-CTA thread-block cluster per tree node.  Each CTA streams an eighth
-// of the node's logits once (float4 loads when aligned), keeping a running
-// maximum and a running sum of exp((z - max) / T) that is rescaled whenever
-// the maximum grows; the CTAs combine their (max, sum) pairs through
-// distributed shared memory.  The uniform u picks the target mass u * S; the
-// CTA whose eighth holds that point finds the warp chunk holding it (chunk
-// sums and their prefix), and that warp walks its chunk 32 logits at a time
-// with a warp scan to find the token.
+// of the node's logits once; each of its warps owns a contiguous run of that
+// eighth (lanes reading it coalesced, eight float4 loads in flight) and
+// keeps running (max, sum of exp((z - max) / T)) pairs, rescaled whenever
+// the maximum grows.  The CTAs combine their pairs through distributed
+// shared memory into the row maximum M and every warp's mass at M.  The
+// uniform u picks the target mass u * S: the CTA, then the warp whose run
+// holds it follow from those masses (one thread per CTA decides, in double:
+// double arithmetic is slow on this GPU); that warp re-reads its run as 32
+// contiguous per-lane pieces, sums each piece, finds the piece holding the
+// target with one warp scan (in double), and that lane walks its piece to
+// the token.
 #include <cooperative_groups.h>
 
 #include <cmath>
@@ -53,25 +57,24 @@ __device__ __forceinline__ uint64_t philox4x64_10_x0(uint64_t x0, uint64_t x1, u
   return x0;
 }
 
-// (m, s) with s = sum exp((z - m) * inv_t): merge another pair into it.
-__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2, float inv_t) {
+// Exponentials in base 2: with c = log2(e) / T, exp((z - m) / T) is
+// 2^((z - m) c), one hardware ex2 (relative error near 2^-22, far below what
+// the draws can resolve).
+__device__ __forceinline__ float exp2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// (m, s) with s = sum 2^((z - m) c): merge another pair into it.
+__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2, float c) {
   if (m2 == -INFINITY) return;
   if (m == -INFINITY) { m = m2; s = s2; return; }
   if (m2 > m) {
-    s = s * expf((m - m2) * inv_t) + s2;
+    s = s * exp2_fast((m - m2) * c) + s2;
     m = m2;
   } else {
-    s += s2 * expf((m2 - m) * inv_t);
-  }
-}
-
-__device__ __forceinline__ void add_logit(float& m, float& s, float z, float inv_t) {
-  if (z == -INFINITY) return;
-  if (z > m) {
-    s = (m == -INFINITY ? 0.f : s * expf((m - z) * inv_t)) + 1.f;
-    m = z;
-  } else {
-    s += expf((z - m) * inv_t);
+    s += s2 * exp2_fast((m2 - m) * c);
   }
 }
 
@@ -79,10 +82,14 @@ __global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kSample
 sample_kernel(const float* __restrict__ logits, int vocab, float inv_t, uint64_t seed,
               uint64_t offset, int32_t* __restrict__ sampled) {
   __shared__ float w_m[kSampleWarps], w_s[kSampleWarps];
-  __shared__ float cta_m;    // this CTA's maximum, read by the cluster
-  __shared__ double cta_s;   // its sum of exp((z - M) / T) at the row maximum M
-  __shared__ double wsum[kSampleWarps];
+  __shared__ double w_mass[kSampleWarps];  // each warp's run's mass at the row maximum
+  __shared__ float cta_m;                  // this CTA's maximum, read by the cluster
+  __shared__ double cta_s;                 // its mass at the row maximum
+  __shared__ float cta_m_row;              // the row maximum
+  __shared__ int sel_owner, sel_warp;      // the drawing CTA and warp (-1: none)
+  __shared__ double sel_rem;               // the target mass left inside that warp's run
   cg::cluster_group cluster = cg::this_cluster();
+  const float c = inv_t * 1.4426950408889634f;  // log2(e) / T
   const int rank = (int)cluster.block_rank();
   const int row = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -90,147 +97,175 @@ sample_kernel(const float* __restrict__ logits, int vocab, float inv_t, uint64_t
   const int beg = min(vocab, rank * chunk);
   const int end = min(vocab, beg + chunk);
   const float* base = logits + (size_t)row * vocab;
+  // warp w's run [wb, we) of this CTA's eighth (a multiple of 4 long)
+  const int wlen = ((end - beg + kSampleWarps * 4 - 1) / (kSampleWarps * 4)) * 4;
+  auto run_begin = [&](int w) { return min(end, beg + w * wlen); };
+  auto run_end = [&](int w) { return min(end, beg + (w + 1) * wlen); };
+  const int wb = run_begin(warp), we = run_end(warp);
 
-  // one pass: running (max, sum) per thread
-  float m = -INFINITY, s = 0.f;
+  // one pass: a running (max, sum) pair per lane, updated once per batch of
+  // 32 loaded logits (the batch's maximum first, then 32 independent
+  // exponentials), so that no lane branches on a new maximum
+  float mm = -INFINITY, ss = 0.f;
+  auto add_batch = [&](const float (&z)[32]) {
+    float bm = z[0];
+#pragma unroll
+    for (int q = 1; q < 32; ++q) bm = fmaxf(bm, z[q]);
+    if (bm == -INFINITY) return;
+    const float mn = fmaxf(mm, bm);
+    float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int q = 0; q < 32; ++q) part[q & 3] += exp2_fast((z[q] - mn) * c);  // 2^-inf = 0
+    ss = (mm == -INFINITY ? 0.f : ss * exp2_fast((mm - mn) * c)) +
+         ((part[0] + part[1]) + (part[2] + part[3]));
+    mm = mn;
+  };
   const bool vec = ((vocab & 3) == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
   if (vec) {
-    // four float4 loads per thread in flight before any is used; logits are
-    // read through L2 (kept: the scan below reads one eighth again)
     const float4* b4 = reinterpret_cast<const float4*>(base);
-    const int e4 = end / 4;
-    for (int i40 = beg / 4 + tid; i40 < e4; i40 += 4 * kSampleThreads) {
-      float4 x[4];
+    const int e4 = we / 4;
+    for (int i40 = wb / 4 + lane; i40 < e4; i40 += 8 * 32) {
+      float z[32];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int i4 = i40 + q * kSampleThreads;
-        x[q] = i4 < e4 ? __ldcg(b4 + i4)
-                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      for (int q = 0; q < 8; ++q) {
+        const int i4 = i40 + q * 32;
+        const float4 x = i4 < e4 ? __ldcg(b4 + i4)
+                                 : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        z[4 * q] = x.x;
+        z[4 * q + 1] = x.y;
+        z[4 * q + 2] = x.z;
+        z[4 * q + 3] = x.w;
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        add_logit(m, s, x[q].x, inv_t);
-        add_logit(m, s, x[q].y, inv_t);
-        add_logit(m, s, x[q].z, inv_t);
-        add_logit(m, s, x[q].w, inv_t);
-      }
+      add_batch(z);
     }
   } else {
-    for (int i = beg + tid; i < end; i += kSampleThreads) add_logit(m, s, __ldcs(base + i), inv_t);
+    for (int i0 = wb + lane; i0 < we; i0 += 32 * 32) {
+      float z[32];
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const int i = i0 + q * 32;
+        z[q] = i < we ? __ldcs(base + i) : -INFINITY;
+      }
+      add_batch(z);
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    merge_ms(m, s, m2, s2, inv_t);
+    const float m2 = __shfl_xor_sync(0xffffffffu, mm, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, ss, o);
+    merge_ms(mm, ss, m2, s2, c);
   }
-  if (lane == 0) { w_m[warp] = m; w_s[warp] = s; }
+  if (lane == 0) { w_m[warp] = mm; w_s[warp] = ss; }
   __syncthreads();
   if (tid == 0) {
-    for (int k = 1; k < kSampleWarps; ++k) merge_ms(m, s, w_m[k], w_s[k], inv_t);
-    cta_m = m;
+    float cm = -INFINITY;
+    for (int k = 0; k < kSampleWarps; ++k) cm = fmaxf(cm, w_m[k]);
+    cta_m = cm;
   }
   cluster.sync();
-  // the row maximum, then this CTA's mass at it
-  float M = -INFINITY;
+  // the row maximum, then every warp's mass and this CTA's mass at it
+  if (tid == 0) {
+    float M = -INFINITY;
 #pragma unroll
-  for (int r = 0; r < kSampleCluster; ++r) M = fmaxf(M, *cluster.map_shared_rank(&cta_m, r));
-  if (tid == 0)
-    cta_s = (m == -INFINITY || M == -INFINITY) ? 0.0 : (double)s * (double)expf((m - M) * inv_t);
+    for (int r = 0; r < kSampleCluster; ++r) M = fmaxf(M, *cluster.map_shared_rank(&cta_m, r));
+    double total = 0.0;
+    for (int k2 = 0; k2 < kSampleWarps; ++k2) {
+      const double wm = (w_m[k2] == -INFINITY || M == -INFINITY)
+                            ? 0.0 : (double)w_s[k2] * (double)exp2_fast((w_m[k2] - M) * c);
+      w_mass[k2] = wm;
+      total += wm;
+    }
+    cta_s = total;
+    cta_m_row = M;
+  }
   cluster.sync();
-  double S = 0.0, P = 0.0, mass[kSampleCluster];
+  // One thread per CTA draws: the CTA whose eighth holds the target mass
+  // u * S (the last one with mass if rounding puts it past the end), then,
+  // in that CTA, the warp whose run holds it.  Doubles are slow on this GPU,
+  // so no other thread touches them here.
+  if (tid == 0) {
+    double S = 0.0, P = 0.0, mass[kSampleCluster];
 #pragma unroll
-  for (int r = 0; r < kSampleCluster; ++r) {
-    mass[r] = *cluster.map_shared_rank(&cta_s, r);
-    S += mass[r];
-  }
-  const uint64_t x0 = philox4x64_10_x0((uint64_t)row, offset, 0ull, 0ull, seed, 0ull);
-  const double u = ((double)(x0 >> 11) + 0.5) * (1.0 / 9007199254740992.0);  // 2^-53
-  const double t = u * S;
-  // the CTA whose eighth holds mass t (the last one with mass if rounding
-  // puts t past the end)
-  int owner = -1, last = -1;
+    for (int r = 0; r < kSampleCluster; ++r) {
+      mass[r] = *cluster.map_shared_rank(&cta_s, r);
+      S += mass[r];
+    }
+    const uint64_t x0 = philox4x64_10_x0((uint64_t)row, offset, 0ull, 0ull, seed, 0ull);
+    const double u = ((double)(x0 >> 11) + 0.5) * (1.0 / 9007199254740992.0);  // 2^-53
+    const double t = u * S;
+    int owner = -1, last = -1;
+    double p_last = 0.0;
 #pragma unroll
-  for (int r = 0; r < kSampleCluster; ++r) {
-    if (mass[r] > 0.0) last = r;
-    if (owner < 0 && mass[r] > 0.0 && P + mass[r] > t) owner = r;
-    if (owner < 0) P += mass[r];
-  }
-  if (last < 0) {  // every logit is -inf: nothing can be drawn
-    if (rank == 0 && tid == 0) sampled[row] = -1;
-  } else if (owner < 0) {
-    owner = last;
-    P = 0.0;
-    for (int r = 0; r < last; ++r) P += mass[r];
-  }
-  if (last >= 0 && rank == owner) {
-    // The eighth in eight contiguous warp chunks (multiples of 32 logits):
-    // each warp sums its chunk with coalesced loads, the chunk holding mass
-    // t is found from the prefix over the warps, and that warp walks it 32
-    // logits at a time with a warp scan.
-    const int len = end - beg;
-    const int wlen = ((len + kSampleWarps * 32 - 1) / (kSampleWarps * 32)) * 32;
-    const int wb = beg + warp * wlen, we = min(end, wb + wlen);
-    auto e_of = [&](float z) { return z == -INFINITY ? 0.f : expf((z - M) * inv_t); };
-    float part = 0.f;
-    for (int v0 = wb; v0 < we; v0 += 32 * 8) {
-      float z[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int v = v0 + 32 * q + lane;
-        z[q] = v < we ? __ldcg(base + v) : -INFINITY;
+    for (int r = 0; r < kSampleCluster; ++r) {
+      if (mass[r] > 0.0) { last = r; p_last = P; }
+      if (owner < 0 && mass[r] > 0.0 && P + mass[r] > t) owner = r;
+      if (owner < 0) P += mass[r];
+    }
+    if (owner < 0) { owner = last; P = p_last; }
+    sel_owner = owner;
+    sel_warp = -1;
+    if (owner == rank) {
+      const double tr = t - P;
+      int pw = -1, lw = -1;
+      double before = 0.0, before_pw = 0.0, before_lw = 0.0;
+      for (int k2 = 0; k2 < kSampleWarps; ++k2) {
+        if (w_mass[k2] > 0.0) { lw = k2; before_lw = before; }
+        if (pw < 0 && w_mass[k2] > 0.0 && before + w_mass[k2] > tr) { pw = k2; before_pw = before; }
+        before += w_mass[k2];
       }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) part += e_of(z[q]);
+      if (pw < 0) { pw = lw; before_pw = before_lw; }  // rounding past the end
+      sel_warp = pw;
+      sel_rem = tr - before_pw;
     }
-    double csum = part;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) csum += __shfl_xor_sync(0xffffffffu, csum, o);
-    if (lane == 0) wsum[warp] = csum;
-    __syncthreads();
-    const double tr = t - P;  // target mass inside this eighth
-    int pw = -1, lw = -1;
-    double before = 0.0, before_pw = 0.0, before_lw = 0.0;
-    for (int k = 0; k < kSampleWarps; ++k) {
-      if (wsum[k] > 0.0) { lw = k; before_lw = before; }
-      if (pw < 0 && wsum[k] > 0.0 && before + wsum[k] > tr) { pw = k; before_pw = before; }
-      before += wsum[k];
-    }
-    if (pw < 0) { pw = lw; before_pw = before_lw; }  // rounding past the end
-    if (warp == pw) {
-      // eight steps of 32 logits are loaded before they are walked
-      double c = before_pw;
-      int tok = -1, lastp = -1;
-      for (int v00 = wb; v00 < we && tok < 0; v00 += 32 * 8) {
-        float e8[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int v = v00 + 32 * q + lane;
-          e8[q] = v < we ? __ldcg(base + v) : -INFINITY;
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int v0 = v00 + 32 * q;
-          if (tok >= 0 || v0 >= we) break;
-          const float e = e_of(e8[q]);
-          float incl = e;  // a scan of 32 terms in float32 on a double base
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-          }
-          const uint32_t cross = __ballot_sync(0xffffffffu, e > 0.f && c + (double)incl > tr);
-          const uint32_t pos = __ballot_sync(0xffffffffu, e > 0.f);
-          if (pos) lastp = v0 + 31 - __clz(pos);
-          if (cross) tok = v0 + __ffs(cross) - 1;
-          c += (double)__shfl_sync(0xffffffffu, incl, 31);
-        }
-      }
-      // rounding past the chunk's mass: its last token with positive mass
-      if (lane == 0) sampled[row] = tok >= 0 ? tok : lastp;
-    }
+    if (last < 0 && rank == 0) sampled[row] = -1;  // every logit is -inf: nothing is drawn
   }
-  cluster.sync();  // no CTA leaves while the others may still read its shared memory
+  // every CTA has read what it needs from the others' shared memory
+  cluster.sync();
+  if (sel_owner != rank || warp != sel_warp) return;
+  const float M = cta_m_row;
+  // 32 contiguous pieces of the run, one per lane
+  auto e_of = [&](float z) { return z == -INFINITY ? 0.f : exp2_fast((z - M) * c); };
+  const int rb = run_begin(warp), re = run_end(warp);
+  const int plen = (re - rb + 31) / 32;
+  const int pb = min(re, rb + lane * plen), pe = min(re, pb + plen);
+  float ls = 0.f;
+  for (int v0 = pb; v0 < pe; v0 += 8) {
+    float z[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) z[q] = v0 + q < pe ? __ldcg(base + v0 + q) : -INFINITY;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) ls += e_of(z[q]);
+  }
+  double incl = ls;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const double rem = sel_rem;  // target mass inside the run
+  const uint32_t cross = __ballot_sync(0xffffffffu, ls > 0.f && incl > rem);
+  const uint32_t pos = __ballot_sync(0xffffffffu, ls > 0.f);
+  if (pos == 0u) {  // nothing left in the run after rounding
+    if (lane == 0) sampled[row] = -1;
+    return;
+  }
+  // the crossing lane, or the last lane with mass if rounding left none; it
+  // walks its piece in float, relative to the piece's start
+  const int wl = cross ? __ffs(cross) - 1 : 31 - __clz(pos);
+  if (lane == wl) {
+    const float target = (float)(rem - (incl - (double)ls));
+    float acc = 0.f;
+    int tok = -1, lastp = -1;
+    for (int v = pb; v < pe; ++v) {
+      const float e = e_of(__ldcg(base + v));
+      if (e > 0.f) {
+        lastp = v;
+        acc += e;
+        if (acc > target) { tok = v; break; }
+      }
+    }
+    sampled[row] = tok >= 0 ? tok : lastp;
+  }
 }
 
 }  // namespace
