@@ -228,13 +228,15 @@ sample_kernel(const float* __restrict__ logits, int vocab, float inv_t, uint64_t
   const int rb = run_begin(warp), re = run_end(warp);
   const int plen = (re - rb + 31) / 32;
   const int pb = min(re, rb + lane * plen), pe = min(re, pb + plen);
+  // (L1-cached loads: the walk below reads the same piece again)
+  constexpr int kBatch = 16;
   float ls = 0.f;
-  for (int v0 = pb; v0 < pe; v0 += 8) {
-    float z[8];
+  for (int v0 = pb; v0 < pe; v0 += kBatch) {
+    float z[kBatch];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) z[q] = v0 + q < pe ? __ldcg(base + v0 + q) : -INFINITY;
+    for (int q = 0; q < kBatch; ++q) z[q] = v0 + q < pe ? __ldg(base + v0 + q) : -INFINITY;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) ls += e_of(z[q]);
+    for (int q = 0; q < kBatch; ++q) ls += e_of(z[q]);
   }
   double incl = ls;
 #pragma unroll
@@ -256,12 +258,18 @@ sample_kernel(const float* __restrict__ logits, int vocab, float inv_t, uint64_t
     const float target = (float)(rem - (incl - (double)ls));
     float acc = 0.f;
     int tok = -1, lastp = -1;
-    for (int v = pb; v < pe; ++v) {
-      const float e = e_of(__ldcg(base + v));
-      if (e > 0.f) {
-        lastp = v;
-        acc += e;
-        if (acc > target) { tok = v; break; }
+    for (int v0 = pb; v0 < pe && tok < 0; v0 += kBatch) {
+      float z[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) z[q] = v0 + q < pe ? __ldg(base + v0 + q) : -INFINITY;
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        const float e = e_of(z[q]);
+        if (tok < 0 && e > 0.f) {
+          lastp = v0 + q;
+          acc += e;
+          if (acc > target) tok = v0 + q;
+        }
       }
     }
     sampled[row] = tok >= 0 ? tok : lastp;
