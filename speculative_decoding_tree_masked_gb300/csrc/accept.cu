@@ -52,25 +52,49 @@ argmax_kernel(const float* __restrict__ logits, int vocab, int32_t* __restrict__
   int bi = INT_MAX;
   const bool vec = ((vocab & 3) == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
   if (vec) {
-    // four float4 loads per thread in flight before any is compared
+    // eight float4 loads per thread in flight; a batch's maximum comes from a
+    // comparison tree and its first occurrence (the lowest index: indices
+    // grow along the batch) from one scan, unless the batch holds a NaN,
+    // which takes the element-wise order
     const float4* b4 = reinterpret_cast<const float4*>(base);
     const int e4 = end / 4;
-    for (int i40 = beg / 4 + tid; i40 < e4; i40 += 4 * kArgmaxThreads) {
-      float4 x[4];
+    for (int i40 = beg / 4 + tid; i40 < e4; i40 += 8 * kArgmaxThreads) {
+      float z[32];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 8; ++q) {
         const int i4 = i40 + q * kArgmaxThreads;
-        x[q] = i4 < e4 ? __ldcs(b4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 x = i4 < e4 ? __ldcs(b4 + i4)
+                                 : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        z[4 * q] = x.x;
+        z[4 * q + 1] = x.y;
+        z[4 * q + 2] = x.z;
+        z[4 * q + 3] = x.w;
       }
+      auto index_of = [&](int k) { return (i40 + (k >> 2) * kArgmaxThreads) * 4 + (k & 3); };
+      bool nan = false;
+      float bm = -INFINITY;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int i4 = i40 + q * kArgmaxThreads;
-        if (i4 >= e4) break;
-        const int i = i4 * 4;
-        if (better(x[q].x, i, bv, bi)) { bv = x[q].x; bi = i; }
-        if (better(x[q].y, i + 1, bv, bi)) { bv = x[q].y; bi = i + 1; }
-        if (better(x[q].z, i + 2, bv, bi)) { bv = x[q].z; bi = i + 2; }
-        if (better(x[q].w, i + 3, bv, bi)) { bv = x[q].w; bi = i + 3; }
+      for (int k = 0; k < 32; ++k) {
+        nan |= isnan(z[k]);
+        bm = fmaxf(bm, z[k]);
+      }
+      if (nan) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          if (i40 + (k >> 2) * kArgmaxThreads < e4 && better(z[k], index_of(k), bv, bi)) {
+            bv = z[k];
+            bi = index_of(k);
+          }
+      } else {
+        int first = 32;
+#pragma unroll
+        for (int k = 31; k >= 0; --k)
+          if (z[k] == bm) first = k;
+        if (first < 32 && i40 + (first >> 2) * kArgmaxThreads < e4 &&
+            better(bm, index_of(first), bv, bi)) {
+          bv = bm;
+          bi = index_of(first);
+        }
       }
     }
   } else {
