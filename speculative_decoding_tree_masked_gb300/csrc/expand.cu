@@ -126,6 +126,47 @@ __device__ __forceinline__ void warp_take(const float (&v)[N], const int (&key)[
   }
 }
 
+// Sorts 8 register-held candidates best first under before() with Knuth's
+// optimal 19-comparator network (empty slots, key < 0, end up last).
+__device__ __forceinline__ void sort8(float (&v)[8], int (&k)[8]) {
+  constexpr int kNet[19][2] = {{0, 2}, {1, 3}, {4, 6}, {5, 7}, {0, 4}, {1, 5}, {2, 6},
+                               {3, 7}, {0, 1}, {2, 3}, {4, 5}, {6, 7}, {2, 4}, {3, 5},
+                               {1, 4}, {3, 6}, {1, 2}, {3, 4}, {5, 6}};
+#pragma unroll
+  for (int c = 0; c < 19; ++c) {
+    const int a = kNet[c][0], b = kNet[c][1];
+    const bool swap = before(v[b], k[b], v[a], k[a]);
+    const float va = v[a], vb = v[b];
+    const int ka = k[a], kb = k[b];
+    v[a] = swap ? vb : va;
+    v[b] = swap ? va : vb;
+    k[a] = swap ? kb : ka;
+    k[b] = swap ? ka : kb;
+  }
+}
+
+// warp_take for 8 candidates per lane: each lane sorts its 8 once, so a round
+// is one warp reduction over the lanes' heads and a register shift in the
+// winning lane (instead of re-scanning its candidates).
+__device__ __forceinline__ void warp_take8(float (&v)[8], int (&key)[8], int r, float* out_v,
+                                           int* out_k) {
+  const int lane = threadIdx.x & 31;
+  sort8(v, key);
+  for (int t = 0; t < r; ++t) {
+    float wv = v[0];
+    int wk = key[0];
+    warp_best(wv, wk);
+    if (lane == 0) { out_v[t] = wv; out_k[t] = wk; }
+    const bool pop = wk >= 0 && wk == key[0];  // this lane held the winner
+#pragma unroll
+    for (int q = 0; q < 7; ++q) {
+      v[q] = pop ? v[q + 1] : v[q];
+      key[q] = pop ? key[q + 1] : key[q];
+    }
+    key[7] = pop ? -1 : key[7];
+  }
+}
+
 // One warp merges nl <= 128 lists held in shared memory, each sorted best
 // first: list l is (vals, keys)[l * stride + 0 .. len), a key < 0 ending it
 // early (keys distinct).  The r best go to out_v / out_k (lane 0 writes).
@@ -240,7 +281,10 @@ expand_chunk_kernel(const float* __restrict__ logits, int vocab, int chunk_len, 
   if (lane == 0) s_red[warp] = sum;
 
   // each warp's w best, then the slice's w best of those
-  warp_take<kPerThread>(z, key, w, s_v + warp * w, s_k + warp * w);
+  if constexpr (kPerThread == 8)
+    warp_take8(z, key, w, s_v + warp * w, s_k + warp * w);
+  else
+    warp_take<kPerThread>(z, key, w, s_v + warp * w, s_k + warp * w);
   __syncthreads();
   if (warp == 0) {
     float* rec = ws + ((size_t)f * gridDim.x + c) * record_words(w);
@@ -290,12 +334,13 @@ expand_merge_kernel(const float* __restrict__ ws, int nf, int chunks, int w,
   for (int f = warp; f < nf; f += kMergeThreads / 32) {
     const float* rows = ws + (size_t)f * chunks * rw;
     const int total = chunks * w;
-    // staged eight loads per lane at a time, all issued before any is stored
-    for (int o0 = 0; o0 < total; o0 += 32 * 8) {
-      float zv[8];
-      int tv[8];
+    // staged 32 loads per lane at a time (all of them when chunks * w <= 1024),
+    // all issued before any is stored
+    for (int o0 = 0; o0 < total; o0 += 32 * 32) {
+      float zv[32];
+      int tv[32];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
+      for (int q = 0; q < 32; ++q) {
         const int o = min(o0 + lane + 32 * q, total - 1);
         const int cc = o / w, k = o - cc * w;
         const float* rec = rows + (size_t)cc * rw;
@@ -303,7 +348,7 @@ expand_merge_kernel(const float* __restrict__ ws, int nf, int chunks, int w,
         tv[q] = reinterpret_cast<const int*>(rec)[3 + 2 * k];
       }
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
+      for (int q = 0; q < 32; ++q) {
         const int o = o0 + lane + 32 * q;
         if (o < total) {
           zl[o] = zv[q];
@@ -311,16 +356,33 @@ expand_merge_kernel(const float* __restrict__ ws, int nf, int chunks, int w,
         }
       }
     }
-    // log-sum-exp: M = max m_c, S = sum s_c e^(m_c - M)
+    // log-sum-exp: M = max m_c, S = sum s_c e^(m_c - M), four slice records
+    // per lane loaded together
     float m = -INFINITY;
-    for (int cc = lane; cc < chunks; cc += 32) m = fmaxf(m, rows[(size_t)cc * rw]);
+    for (int c0 = 0; c0 < chunks; c0 += 128) {
+      float rm[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int cc = c0 + lane + 32 * q;
+        rm[q] = cc < chunks ? rows[(size_t)cc * rw] : -INFINITY;
+      }
+      m = fmaxf(m, fmaxf(fmaxf(rm[0], rm[1]), fmaxf(rm[2], rm[3])));
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float sum = 0.f;
     if (m != -INFINITY)
-      for (int cc = lane; cc < chunks; cc += 32) {
-        const float* rec = rows + (size_t)cc * rw;
-        if (rec[0] != -INFINITY) sum += rec[1] * __expf(rec[0] - m);
+      for (int c0 = 0; c0 < chunks; c0 += 128) {
+        float rm[4], rs[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int cc = c0 + lane + 32 * q;
+          rm[q] = cc < chunks ? rows[(size_t)cc * rw] : -INFINITY;
+          rs[q] = cc < chunks ? rows[(size_t)cc * rw + 1] : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (rm[q] != -INFINITY) sum += rs[q] * __expf(rm[q] - m);
       }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
