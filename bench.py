@@ -478,12 +478,64 @@ SWEEP_PREFIXES = (1024, 4096, 16384, 32768)
 SWEEP_NODES = (8, 32, 64, 128)
 
 
+def _sdpa_us(q, ks, vs, prefix, parent, copies, reps, warmup, stream, masked=True):
+    """The same attention through PyTorch's scaled_dot_product_attention (GQA
+    expanded by the library), timed like the kernel, for context.  masked:
+    the ancestor mask as a boolean attn_mask (the library's masked path);
+    unmasked: every node sees every prefix and tree key, which the fastest
+    (flash-class) backends take -- a floor for a mask-free attention kernel
+    over the same keys."""
+    import numpy as np
+    import torch
+    import torch.nn.functional as F
+
+    n = q.shape[0]
+    vis = np.ones((n, prefix + n), dtype=bool)
+    tree = np.zeros((n, n), dtype=bool)
+    for i in range(n):
+        u = i
+        while u >= 0:
+            tree[i, u] = True
+            u = int(parent[u])
+    vis[:, prefix:] = tree
+    mask = torch.from_numpy(vis).to(q.device)
+    qs = q.permute(1, 0, 2).unsqueeze(0)
+    kv = [(k[:, :prefix + n].unsqueeze(0), v[:, :prefix + n].unsqueeze(0))
+          for k, v in zip(ks, vs)]
+
+    def calls():
+        for k, v in kv:
+            F.scaled_dot_product_attention(qs, k, v, attn_mask=mask if masked else None,
+                                           enable_gqa=True)
+
+    try:
+        with torch.cuda.stream(stream):
+            calls()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            calls()
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                graph.replay()
+            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ea.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            eb.record(stream)
+        torch.cuda.synchronize()
+        return ea.elapsed_time(eb) * 1e3 / (reps * copies)
+    except RuntimeError as e:  # a backend that does not take these shapes
+        return f"unavailable: {str(e).splitlines()[0][:120]}"
+
+
 def run_sweep(args, local_rank):
     """Attention alone over the context/tree sweep at Qwen2-72B-class shapes
     (64/8 heads, d128, bf16, random-parent trees of depth <= 16): one JSON
     line per (prefix, nodes).  Each configuration cycles through enough
     device copies of its KV cache that they exceed L2 several times over, in
-    a CUDA graph timed with events on its stream."""
+    a CUDA graph timed with events on its stream; PyTorch's masked SDPA on
+    the same inputs is timed beside it for context."""
     import torch
 
     import speculative_decoding_tree_masked_gb300 as tvp
@@ -534,6 +586,9 @@ def run_sweep(args, local_rank):
             if int(status.item()) != 0:
                 raise RuntimeError(f"device status {int(status.item())} in the sweep")
             us = ea.elapsed_time(eb) * 1e3 / (reps * copies)
+            sdpa_us = _sdpa_us(q, ks, vs, prefix, w.parent, copies, reps, args.warmup, stream)
+            flash_us = _sdpa_us(q, ks, vs, prefix, w.parent, copies, reps, args.warmup, stream,
+                                masked=False)
             nbytes, flops = _algorithmic_work(w.parent, prefix, n, w.hq, w.hkv, w.d)
             bounds = _bounds_us(nbytes, flops, _visible_pairs(w.parent, prefix, w.hq), peaks)
             binding = max(bounds, key=bounds.get)
@@ -545,6 +600,7 @@ def run_sweep(args, local_rank):
                 "tflops": flops / us / 1e6, "tensor_frac": flops / us / 1e6 / peaks["bf16_tflops"],
                 "bounds_us": bounds, "bound": binding, "binding_frac": bounds[binding] / us,
                 "splits": _splits_for(tvp, n, w.hq, w.hkv, w.d, prefix),
+                "torch_sdpa_masked_us": sdpa_us, "torch_sdpa_unmasked_us": flash_us,
                 "kv_copies": copies, "peak_source": peaks["source"]}), flush=True)
         del ks, vs, k0, v0
         torch.cuda.empty_cache()
