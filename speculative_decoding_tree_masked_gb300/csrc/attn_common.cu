@@ -145,6 +145,10 @@ template <typename PT, typename T, int D, int S>
 __global__ void __launch_bounds__(256) combine_kernel(const uint8_t* __restrict__ ws, int splits,
                                                       int rows, T* __restrict__ out) {
   constexpr int C = D / 32;  // consecutive columns per lane
+  // the next layer's attention kernel (launched under programmatic
+  // serialization) may start its setup now; it waits for this grid to
+  // finish before it reads or writes memory
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;

@@ -327,6 +327,11 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
     ptx::tmem_relinquish();
   }
+  // Everything above reads nothing an earlier kernel may write.  The kernel
+  // is launched under programmatic stream serialization, so it may start
+  // while the previous kernel (the last layer's combine, say) finishes; it
+  // waits for that grid here, before its first global read or write.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid == 0 && p.q_tma) {
     // A tile's 128 rows are 128/G consecutive nodes x the G query heads of
     // KV head g: one box per 64-column chunk over Q seen as [N][Hq][d], in
@@ -854,6 +859,26 @@ cudaError_t set_smem_attr() {
   return cudaSuccess;
 }
 
+// Launches the attention kernel with programmatic stream serialization: it
+// may begin its setup before the previous kernel on the stream has finished
+// (that kernel must signal griddepcontrol.launch_dependents, as the combine
+// does) and waits for it with griddepcontrol.wait before touching memory.
+template <typename Arg>
+cudaError_t launch_early(void (*kernel)(Arg), dim3 grid, uint32_t smem, cudaStream_t s,
+                         const Arg& arg) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, arg);
+}
+
 // The tensor maps and parameters of one request under its split plan.
 template <int D>
 bool fill_request(const AttnProblem& p, const SplitPlan& plan, float* ws, CUtensorMap* kmap,
@@ -913,8 +938,7 @@ cudaError_t launch_d(const AttnProblem& p, const SplitPlan& plan, float* ws, cud
                        &batch.omap[0], &batch.req[0]))
     return cudaErrorInvalidValue;
   const dim3 grid(plan.splits, plan.row_tiles, p.hkv);
-  attn_tc_kernel<D, 1, PAGED><<<grid, kThreads, Layout<D, PAGED>::kAlloc, s>>>(batch);
-  return cudaGetLastError();
+  return launch_early(attn_tc_kernel<D, 1, PAGED>, grid, Layout<D, PAGED>::kAlloc, s, batch);
 }
 
 template <int D, bool PAGED>
@@ -938,11 +962,13 @@ cudaError_t launch_batched_d(const AttnProblem* probs, const SplitPlan* plans, i
           if (ok) batch->cta[ctas++] = pack_cta(b, g, rg, sp);
         }
   }
+  cudaError_t le = cudaSuccess;
   if (ok)
-    attn_tc_kernel<D, kMaxBatch, PAGED><<<ctas, kThreads, Layout<D, PAGED>::kAlloc, s>>>(*batch);
+    le = launch_early(attn_tc_kernel<D, kMaxBatch, PAGED>, dim3(ctas), Layout<D, PAGED>::kAlloc, s,
+                      *batch);
   delete batch;
   if (!ok) return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  return le;
 }
 
 }  // namespace
