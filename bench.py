@@ -114,7 +114,10 @@ class _Clocks:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        # the raw samples go to TV_CLOCKS_DIR (default: the temporary directory)
+        import tempfile
+        folder = os.environ.get("TV_CLOCKS_DIR", tempfile.gettempdir())
+        self.path = os.path.join(folder, f"clocks_rank{index}.csv")
 
     def __enter__(self):
         try:
