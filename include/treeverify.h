@@ -234,7 +234,7 @@ TV_API tv_status tv_tree_attn_verify_batched(int32_t batch, const void* const* q
  * share one pool and each has its own table, so prefixes need no contiguous
  * room and whole pages can be shared or recycled.  Passage: the same as
  * tv_tree_attn_verify; paging is the serving form of its cache layout (the
- * page verifies one request).
+ * review page verifies one request).
  *
  * Contract for every paged call:
  *   page_size     a multiple of 64 (a key block is two 64-row boxes)
