@@ -148,6 +148,12 @@ TV_API int32_t tv_attn_uses_tensor_cores(int32_t dtype);
  *
  * All device pointers must be 16-byte aligned.  Rows of one KV head are
  * d elements apart and heads cap * d elements apart.
+ *
+ * The bf16 kernel is launched with programmatic stream serialization: it may
+ * begin its setup before the previous kernel on the stream has finished (if
+ * that kernel allows it, as this library's split merge does), and it waits
+ * for that kernel to complete before it reads or writes any memory, so
+ * stream order holds for every buffer.
  */
 TV_API tv_status tv_tree_attn_verify(const void* q, const void* k_cache, const void* v_cache,
                               int64_t cap, int32_t prefix_len, int32_t n_nodes,
