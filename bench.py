@@ -731,8 +731,10 @@ def run_batch(args, local_rank):
     """Batched tree attention: 8 requests at 70B-class shapes (64/8 heads,
     d128, bf16, 64-node trees) with ragged prefixes 1K, 2K, ..., 8K, one
     layer each, as one batched call and as 8 single calls; every layer has
-    its own caches and three layers are cycled (larger than L2).  One JSON
-    line."""
+    its own caches and three layers are cycled (larger than L2).  Then the
+    rest of the step for the same 8 requests: acceptance over their packed
+    logits (8 x 64 rows of 128256, planted argmax) and the compaction of
+    the three layers, batched against per-request calls.  Two JSON lines."""
     import numpy as np
     import torch
 
@@ -777,8 +779,8 @@ def run_batch(args, local_rank):
                 tvp.tree_attn_verify(r[0], r[1][l], r[2][l], r[3], r[4], out=outs[b],
                                      workspace=ws_s[b], status=status)
 
-    res = {}
-    for name, fn in (("batched", batched), ("single_calls", singles)):
+    def graph_us(fn):
+        """Microseconds per replay of fn captured as one CUDA graph."""
         with torch.cuda.stream(stream):
             fn()
         torch.cuda.synchronize()
@@ -795,7 +797,10 @@ def run_batch(args, local_rank):
                 graph.replay()
             eb.record(stream)
         torch.cuda.synchronize()
-        res[name] = ea.elapsed_time(eb) * 1e3 / (reps * layers)
+        return ea.elapsed_time(eb) * 1e3 / reps
+
+    res = {name: graph_us(fn) / layers
+           for name, fn in (("batched", batched), ("single_calls", singles))}
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in the batch")
     print(json.dumps({
@@ -806,6 +811,49 @@ def run_batch(args, local_rank):
         "tflops": {k: flops / v / 1e6 for k, v in res.items()},
         "tensor_frac": {k: flops / v / 1e6 / peaks["bf16_tflops"] for k, v in res.items()},
         "hbm_frac": {k: nbytes / v / 1e3 / peaks["hbm_gbs"] for k, v in res.items()},
+        "peak_source": peaks["source"]}), flush=True)
+
+    # acceptance and compaction of the same requests
+    ws_acc = [synth.make_workload("full_step", seed=args.seed + b, planted_m=b, layers=1)
+              for b in range(len(prefixes))]
+    ns = [NODES] * len(prefixes)
+    cat = lambda xs: torch.from_numpy(np.ascontiguousarray(np.concatenate(xs))).to(dev)
+    logits = cat([w.logits for w in ws_acc])
+    token = cat([w.token.astype(np.int32) for w in ws_acc])
+    parent = cat([w.parent.astype(np.int32) for w in ws_acc])
+    acc = tvp.tree_accept_batched(logits, token, parent, ns, prefixes, status=status)
+    sl = lambda t, b: t[b * NODES:(b + 1) * NODES]
+    acc1 = [tvp.tree_accept(sl(logits, b), sl(token, b), sl(parent, b), P, status=status)
+            for b, P in enumerate(prefixes)]
+
+    def accept_batched():
+        tvp.tree_accept_batched(logits, token, parent, ns, prefixes, outs=acc, status=status)
+        for l in range(layers):
+            tvp.kv_compact_batched([r[1][l] for r in reqs], [r[2][l] for r in reqs], prefixes,
+                                   ns, acc["new_pos"], status=status)
+
+    def accept_singles():
+        for b, P in enumerate(prefixes):
+            tvp.tree_accept(sl(logits, b), sl(token, b), sl(parent, b), P, outs=acc1[b],
+                            status=status)
+            for l in range(layers):
+                tvp.kv_compact(reqs[b][1][l], reqs[b][2][l], P, NODES, acc1[b]["new_pos"],
+                               status=status)
+
+    res = {name: graph_us(fn) for name, fn in (("batched", accept_batched),
+                                               ("single_calls", accept_singles))}
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the batched acceptance")
+    m = acc["m"].cpu().tolist()
+    if m != [int(w.planted_path.size) - 1 for w in ws_acc]:
+        raise RuntimeError(f"accepted lengths {m} differ from the planted ones")
+    print(json.dumps({
+        "kernel": "batched acceptance + compaction (argmax, walk, 3 layers of KV moves)",
+        "workload": "8 requests, 64-node trees, V=128256 fp32 logits, planted m = 0..7, "
+                    "64/8 heads, d128, bf16 caches at prefixes 1K..8K",
+        "us_per_step": res, "accepted_m": m,
+        "logits_hbm_frac": {k: logits.numel() * 4 / v / 1e3 / peaks["hbm_gbs"]
+                            for k, v in res.items()},
         "peak_source": peaks["source"]}), flush=True)
 
 

@@ -418,6 +418,85 @@ TV_API tv_status tv_kv_compact(void* k_cache, void* v_cache, int32_t n_layers,
                         const int32_t* new_pos, int32_t* dev_status, tv_stream_t stream);
 
 /*
+ * Batched acceptance and compaction: the rest of a verification step for up
+ * to TV_MAX_BATCH requests at once, beside tv_tree_attn_verify_batched.
+ * Same passages as tv_tree_accept and tv_kv_compact; every request's results
+ * are exactly (bit for bit) what the single-request calls give for it.
+ *
+ * Packed node arrays.  node_offset is a HOST int32 array of batch + 1
+ * entries, node_offset[0] = 0: request b owns entries
+ * [node_offset[b], node_offset[b + 1]) of every per-node device array
+ * (logits rows, token, parent, am, path, new_pos, new_parent), with 1 to
+ * TV_MAX_NODES nodes, and its parent entries are indices within the request
+ * (node 0 is its root).  m and n_survivors hold one entry per request;
+ * request b's n_b + 1 out_tokens start at entry node_offset[b] + b.
+ * prefix_len is a HOST int32 array of batch entries.  A tree or token error
+ * in one request is reported in dev_status and leaves that request's
+ * outputs as tv_tree_accept leaves them; the other requests are unaffected.
+ */
+
+/* tv_tree_accept over packed requests: logits device float32
+ * [node_offset[batch]][vocab], one argmax pass over all rows, then one walk
+ * per request.  Host-side errors as tv_tree_accept, plus TV_ERR_INVALID_ARG
+ * for batch outside [1, TV_MAX_BATCH] or a bad node_offset. */
+TV_API tv_status tv_tree_accept_batched(int32_t batch, const int32_t* node_offset,
+                                        const int32_t* prefix_len, const float* logits,
+                                        int32_t vocab, const int32_t* token,
+                                        const int32_t* parent, int32_t* am, int32_t* m,
+                                        int32_t* path, int32_t* out_tokens, int32_t* new_pos,
+                                        int32_t* new_parent, int32_t* n_survivors,
+                                        int32_t* dev_status, tv_stream_t stream);
+
+/* tv_tree_accept_tokens over packed requests (target_token packed like
+ * token). */
+TV_API tv_status tv_tree_accept_tokens_batched(int32_t batch, const int32_t* node_offset,
+                                               const int32_t* prefix_len,
+                                               const int32_t* target_token, int32_t vocab,
+                                               const int32_t* token, const int32_t* parent,
+                                               int32_t* m, int32_t* path, int32_t* out_tokens,
+                                               int32_t* new_pos, int32_t* new_parent,
+                                               int32_t* n_survivors, int32_t* dev_status,
+                                               tv_stream_t stream);
+
+/*
+ * tv_kv_compact for `batch` requests in one launch.  HOST arrays of `batch`
+ * entries:
+ *   k_cache, v_cache     device bases of layer 0 of request b's caches,
+ *                        [n_layers][hkv][cap[b]][d] with layer l at element
+ *                        offset l * layer_stride_elems[b]
+ *   layer_stride_elems   >= hkv * cap[b] * d
+ *   cap, prefix_len, n_nodes   as tv_kv_compact, per request
+ *   new_pos              device pointers, request b's new_pos [n_nodes[b]]
+ *                        (for packed acceptance outputs: new_pos +
+ *                        node_offset[b])
+ * n_layers, hkv, d and dtype are shared.  The rows
+ * [prefix_len[b], prefix_len[b] + n_nodes[b]) of different requests must not
+ * overlap in memory (they are moved concurrently).  Every check of
+ * tv_kv_compact applies to every request and is made before the launch.
+ */
+TV_API tv_status tv_kv_compact_batched(int32_t batch, void* const* k_cache,
+                                       void* const* v_cache, const int64_t* layer_stride_elems,
+                                       const int64_t* cap, const int32_t* prefix_len,
+                                       const int32_t* n_nodes, const int32_t* const* new_pos,
+                                       int32_t n_layers, int32_t hkv, int32_t d, int32_t dtype,
+                                       int32_t* dev_status, tv_stream_t stream);
+
+/* tv_kv_compact_paged for `batch` requests sharing one page pool per layer:
+ * page_table, prefix_len, n_nodes and new_pos are HOST arrays of `batch`
+ * entries (page_table[b] and new_pos[b] device pointers).  No page may hold
+ * tree rows [prefix_len[b], prefix_len[b] + n_nodes[b]) of one request and
+ * any row of another; prefix pages may be shared, since compaction never
+ * writes below prefix_len. */
+TV_API tv_status tv_kv_compact_batched_paged(int32_t batch, void* k_pool, void* v_pool,
+                                             int32_t n_layers, int64_t layer_stride_elems,
+                                             int32_t num_pages, int32_t hkv, int32_t page_size,
+                                             int32_t d, int32_t dtype,
+                                             const int32_t* const* page_table,
+                                             const int32_t* prefix_len, const int32_t* n_nodes,
+                                             const int32_t* const* new_pos, int32_t* dev_status,
+                                             tv_stream_t stream);
+
+/*
  * The draft side.  These two calls serve the draft model that proposes the
  * trees; they are not part of the target's verification step.
  */

@@ -387,6 +387,178 @@ def kv_compact(k_cache: torch.Tensor, v_cache: torch.Tensor, prefix_len: int, n_
         "tv_kv_compact")
 
 
+# ------------------------------------------------- batched acceptance, compaction
+
+def node_offsets(n_nodes) -> list:
+    """The packed layout's offsets: [0, n_0, n_0 + n_1, ...]."""
+    off = [0]
+    for n in n_nodes:
+        off.append(off[-1] + int(n))
+    return off
+
+
+def _packed_outs(names, n_nodes, device) -> dict:
+    off = node_offsets(n_nodes)
+    total, batch = off[-1], len(n_nodes)
+    sizes = {"am": total, "sampled": total, "m": batch, "path": total,
+             "out_tokens": total + batch, "new_pos": total, "new_parent": total,
+             "n_survivors": batch}
+    return {k: torch.empty(sizes[k], dtype=torch.int32, device=device) for k in names}
+
+
+def _check_packed(n_nodes, prefix_lens, *per_node):
+    if len(n_nodes) != len(prefix_lens):
+        raise ValueError("n_nodes and prefix_lens differ in length")
+    total = sum(int(n) for n in n_nodes)
+    for t in per_node:
+        if t.dtype != torch.int32 or t.numel() != total:
+            raise ValueError("packed per-node arrays must be int32 [sum(n_nodes)]")
+    return node_offsets(n_nodes)
+
+
+def tree_accept_batched(logits: torch.Tensor, token: torch.Tensor, parent: torch.Tensor,
+                        n_nodes, prefix_lens, outs: Optional[dict] = None,
+                        status: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """Greedy acceptance of several requests over packed node arrays: request
+    b owns rows off[b] .. off[b + 1] - 1 of logits [total][V], token [total]
+    and parent [total] (its parent entries index its own nodes), where off =
+    node_offsets(n_nodes).  Returns a dict of packed int32 tensors: am [total],
+    m [B], path [total], out_tokens [total + B] (request b's n_b + 1 entries
+    from off[b] + b), new_pos [total], new_parent [total], n_survivors [B];
+    batched_request(outs, b) gives request b's part in tree_accept's form."""
+    _need_cuda(logits, token, parent)
+    total, vocab = logits.shape
+    off = _check_packed(n_nodes, prefix_lens, token, parent)
+    if logits.dtype != torch.float32 or off[-1] != total:
+        raise ValueError("logits must be float32 [sum(n_nodes)][V]")
+    if outs is None:
+        outs = _packed_outs(("am", "m", "path", "out_tokens", "new_pos", "new_parent",
+                             "n_survivors"), n_nodes, logits.device)
+    offs = _host_array(ctypes.c_int32, off)
+    pre = _host_array(ctypes.c_int32, [int(x) for x in prefix_lens])
+    _check(lib().tv_tree_accept_batched(
+        len(n_nodes), ctypes.cast(offs, ctypes.c_void_p), ctypes.cast(pre, ctypes.c_void_p),
+        _ptr(logits), vocab, _ptr(token), _ptr(parent), _ptr(outs["am"]), _ptr(outs["m"]),
+        _ptr(outs["path"]), _ptr(outs["out_tokens"]), _ptr(outs["new_pos"]),
+        _ptr(outs["new_parent"]), _ptr(outs["n_survivors"]), _ptr(status),
+        _stream(stream, logits.device)), "tv_tree_accept_batched")
+    outs["node_offset"] = off
+    return outs
+
+
+def tree_accept_tokens_batched(target_token: torch.Tensor, vocab: int, token: torch.Tensor,
+                               parent: torch.Tensor, n_nodes, prefix_lens,
+                               outs: Optional[dict] = None,
+                               status: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """tree_accept_batched with the target's token at every packed node given
+    instead of logits.  Returns its dict without "am"."""
+    _need_cuda(target_token, token, parent)
+    off = _check_packed(n_nodes, prefix_lens, target_token, token, parent)
+    if outs is None:
+        outs = _packed_outs(("m", "path", "out_tokens", "new_pos", "new_parent",
+                             "n_survivors"), n_nodes, parent.device)
+    offs = _host_array(ctypes.c_int32, off)
+    pre = _host_array(ctypes.c_int32, [int(x) for x in prefix_lens])
+    _check(lib().tv_tree_accept_tokens_batched(
+        len(n_nodes), ctypes.cast(offs, ctypes.c_void_p), ctypes.cast(pre, ctypes.c_void_p),
+        _ptr(target_token), vocab, _ptr(token), _ptr(parent), _ptr(outs["m"]),
+        _ptr(outs["path"]), _ptr(outs["out_tokens"]), _ptr(outs["new_pos"]),
+        _ptr(outs["new_parent"]), _ptr(outs["n_survivors"]), _ptr(status),
+        _stream(stream, parent.device)), "tv_tree_accept_tokens_batched")
+    outs["node_offset"] = off
+    return outs
+
+
+def batched_request(outs: dict, b: int) -> dict:
+    """Request b's results from a packed batched-acceptance dict, as views
+    shaped like tree_accept's."""
+    off = outs["node_offset"]
+    lo, hi = off[b], off[b + 1]
+    r = {k: outs[k][lo:hi] for k in ("am", "sampled", "path", "new_pos", "new_parent")
+         if k in outs}
+    r["out_tokens"] = outs["out_tokens"][lo + b:hi + b + 1]
+    r["m"] = outs["m"][b:b + 1]
+    r["n_survivors"] = outs["n_survivors"][b:b + 1]
+    return r
+
+
+def _per_request_new_pos(new_pos, n_nodes) -> list:
+    """A packed int32 tensor (sliced at node_offsets) or a list of tensors."""
+    if isinstance(new_pos, torch.Tensor):
+        off = node_offsets(n_nodes)
+        if new_pos.numel() != off[-1]:
+            raise ValueError("packed new_pos must hold sum(n_nodes) entries")
+        new_pos = [new_pos[off[b]:off[b + 1]] for b in range(len(n_nodes))]
+    if len(new_pos) != len(n_nodes):
+        raise ValueError("one new_pos per request")
+    for t, n in zip(new_pos, n_nodes):
+        if t.dtype != torch.int32 or t.numel() != int(n):
+            raise ValueError("new_pos must be int32 [n_nodes]")
+    return list(new_pos)
+
+
+def kv_compact_batched(k_caches, v_caches, prefix_lens, n_nodes, new_pos,
+                       status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """kv_compact for several requests in one launch: lists of per-request
+    caches [L][Hkv][cap_b][d] (or [Hkv][cap_b][d]), prefix lengths and tree
+    sizes; new_pos packed (the new_pos of tree_accept_batched) or a list."""
+    batch = len(k_caches)
+    if not (len(v_caches) == len(prefix_lens) == len(n_nodes) == batch):
+        raise ValueError("per-request lists differ in length")
+    new_pos = _per_request_new_pos(new_pos, n_nodes)
+    _need_cuda(*k_caches, *v_caches, *new_pos)
+    shapes = []
+    for k, v in zip(k_caches, v_caches):
+        if k.shape != v.shape or k.dtype != v.dtype or k.dtype != k_caches[0].dtype:
+            raise ValueError("k and v caches differ")
+        if not k.is_contiguous() or not v.is_contiguous():
+            raise ValueError("caches must be contiguous")
+        shapes.append(k.shape if k.dim() == 4 else (1,) + tuple(k.shape))
+    layers, hkv, _, d = shapes[0]
+    if any(s[0] != layers or s[1] != hkv or s[3] != d for s in shapes):
+        raise ValueError("layers, heads and d must agree")
+    vp = lambda ts: _host_array(ctypes.c_void_p, [_ptr(t) for t in ts])
+    arrs = [vp(k_caches), vp(v_caches),
+            _host_array(ctypes.c_int64, [hkv * s[2] * d for s in shapes]),
+            _host_array(ctypes.c_int64, [s[2] for s in shapes]),
+            _host_array(ctypes.c_int32, [int(x) for x in prefix_lens]),
+            _host_array(ctypes.c_int32, [int(x) for x in n_nodes]), vp(new_pos)]
+    cp = [ctypes.cast(a, ctypes.c_void_p) for a in arrs]
+    _check(lib().tv_kv_compact_batched(
+        batch, cp[0], cp[1], cp[2], cp[3], cp[4], cp[5], cp[6], layers, hkv, d,
+        _dtype_code(k_caches[0]), _ptr(status), _stream(stream, k_caches[0].device)),
+        "tv_kv_compact_batched")
+
+
+def kv_compact_batched_paged(k_pools: torch.Tensor, v_pools: torch.Tensor, page_tables,
+                             prefix_lens, n_nodes, new_pos,
+                             status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """kv_compact_paged for several requests sharing one pool per layer
+    ([L][num_pages][Hkv][page_size][d], or without L): one page table per
+    request; new_pos packed or a list."""
+    batch = len(page_tables)
+    if not (len(prefix_lens) == len(n_nodes) == batch):
+        raise ValueError("per-request lists differ in length")
+    new_pos = _per_request_new_pos(new_pos, n_nodes)
+    _need_cuda(k_pools, v_pools, *page_tables, *new_pos)
+    if k_pools.shape != v_pools.shape or k_pools.dtype != v_pools.dtype:
+        raise ValueError("k and v pools differ")
+    if not k_pools.is_contiguous() or not v_pools.is_contiguous():
+        raise ValueError("pools must be contiguous")
+    shape = k_pools.shape if k_pools.dim() == 5 else (1,) + tuple(k_pools.shape)
+    layers, num_pages, hkv, page_size, d = shape
+    if any(t.dtype != torch.int32 for t in page_tables):
+        raise ValueError("page tables must be int32")
+    vp = lambda ts: _host_array(ctypes.c_void_p, [_ptr(t) for t in ts])
+    arrs = [vp(page_tables), _host_array(ctypes.c_int32, [int(x) for x in prefix_lens]),
+            _host_array(ctypes.c_int32, [int(x) for x in n_nodes]), vp(new_pos)]
+    cp = [ctypes.cast(a, ctypes.c_void_p) for a in arrs]
+    _check(lib().tv_kv_compact_batched_paged(
+        batch, _ptr(k_pools), _ptr(v_pools), layers, num_pages * hkv * page_size * d, num_pages,
+        hkv, page_size, d, _dtype_code(k_pools), cp[0], cp[1], cp[2], cp[3], _ptr(status),
+        _stream(stream, k_pools.device)), "tv_kv_compact_batched_paged")
+
+
 # ---------------------------------------------------------------- draft side
 
 def expand_workspace(n_frontier: int, vocab: int, w: int, device) -> torch.Tensor:

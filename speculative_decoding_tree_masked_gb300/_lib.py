@@ -51,6 +51,16 @@ SIGNATURES = {
     "tv_tree_accept_sampled": (c_i32, [c_ptr, c_i32, c_ptr, c_ptr, c_i32, c_i32, ctypes.c_float,
                                        ctypes.c_uint64, ctypes.c_uint64, c_ptr, c_ptr, c_ptr,
                                        c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr]),
+    "tv_tree_accept_batched": (c_i32, [c_i32, c_ptr, c_ptr, c_ptr, c_i32, c_ptr, c_ptr, c_ptr,
+                                       c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr]),
+    "tv_tree_accept_tokens_batched": (c_i32, [c_i32, c_ptr, c_ptr, c_ptr, c_i32, c_ptr, c_ptr,
+                                              c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr,
+                                              c_ptr]),
+    "tv_kv_compact_batched": (c_i32, [c_i32, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr,
+                                      c_i32, c_i32, c_i32, c_i32, c_ptr, c_ptr]),
+    "tv_kv_compact_batched_paged": (c_i32, [c_i32, c_ptr, c_ptr, c_i32, c_i64, c_i32, c_i32,
+                                            c_i32, c_i32, c_i32, c_ptr, c_ptr, c_ptr, c_ptr,
+                                            c_ptr, c_ptr]),
     "tv_expand_workspace_size": (c_size, [c_i32, c_i32, c_i32]),
     "tv_tree_expand": (c_i32, [c_ptr, c_i32, c_i32, c_ptr, c_ptr, c_i32, c_i32, c_ptr, c_ptr,
                                c_ptr, c_ptr, c_size, c_ptr, c_ptr]),

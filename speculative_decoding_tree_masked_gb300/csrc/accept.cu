@@ -5,6 +5,8 @@
 // aligned) and the partial winners meet in CTA 0 through distributed shared
 // memory.  walk: one warp walks the tree with ballots (lane k holds nodes
 // k, k+32, k+64, k+96) and builds the re-root map with ballot/popc ranks.
+// Several requests are verified at once by packing their node arrays: the
+// argmax runs over all packed rows and one warp walks each request.
 #include <cooperative_groups.h>
 
 #include <climits>
@@ -129,14 +131,35 @@ argmax_kernel(const float* __restrict__ logits, int vocab, int32_t* __restrict__
   cluster.sync();  // keep every CTA's shared memory alive until CTA 0 has read it
 }
 
+// Request b of a packed batch owns nodes [off[b], off[b + 1]) of every
+// per-node array; its m and n_survivors are entry b, its out_tokens start at
+// off[b] + b (n_b + 1 entries each).
+struct WalkJobs {
+  int32_t off[kMaxBatch + 1];
+  int32_t prefix[kMaxBatch];
+};
+
 __global__ void __launch_bounds__(32)
-walk_kernel(const int32_t* __restrict__ token, const int32_t* __restrict__ parent,
-            const int32_t* __restrict__ am, int n, int vocab, int prefix, int32_t* m_out,
-            int32_t* path, int32_t* out_tokens, int32_t* new_pos, int32_t* new_parent,
-            int32_t* n_surv, int32_t* dev_status) {
+walk_kernel(const __grid_constant__ WalkJobs jobs, const int32_t* __restrict__ token_all,
+            const int32_t* __restrict__ parent_all, const int32_t* __restrict__ am_all,
+            int vocab, int32_t* m_out, int32_t* path, int32_t* out_tokens, int32_t* new_pos,
+            int32_t* new_parent, int32_t* n_surv, int32_t* dev_status) {
   __shared__ int32_t par[kMaxNodes], tok[kMaxNodes], amv[kMaxNodes], rank_of[kMaxNodes];
   __shared__ int32_t plist[kMaxNodes];
   const int lane = threadIdx.x;
+  const int b = blockIdx.x;
+  const int o = jobs.off[b];
+  const int n = jobs.off[b + 1] - o;
+  const int prefix = jobs.prefix[b];
+  const int32_t* token = token_all + o;
+  const int32_t* parent = parent_all + o;
+  const int32_t* am = am_all + o;
+  m_out += b;
+  n_surv += b;
+  path += o;
+  out_tokens += o + b;
+  new_pos += o;
+  new_parent += o;
   bool ok = true;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -246,19 +269,47 @@ cudaError_t launch_accept(const float* logits, int32_t vocab, const int32_t* tok
                           int32_t* m, int32_t* path, int32_t* out_tokens, int32_t* new_pos,
                           int32_t* new_parent, int32_t* n_survivors, int32_t* dev_status,
                           cudaStream_t s) {
-  argmax_kernel<<<dim3(kArgmaxCluster, n), kArgmaxThreads, 0, s>>>(logits, vocab, am);
+  const int32_t off[2] = {0, n};
+  return launch_accept_batched(logits, vocab, token, parent, 1, off, &prefix, am, m, path,
+                               out_tokens, new_pos, new_parent, n_survivors, dev_status, s);
+}
+
+cudaError_t launch_accept_batched(const float* logits, int32_t vocab, const int32_t* token,
+                                  const int32_t* parent, int32_t batch,
+                                  const int32_t* node_offset, const int32_t* prefix,
+                                  int32_t* am, int32_t* m, int32_t* path, int32_t* out_tokens,
+                                  int32_t* new_pos, int32_t* new_parent, int32_t* n_survivors,
+                                  int32_t* dev_status, cudaStream_t s) {
+  argmax_kernel<<<dim3(kArgmaxCluster, node_offset[batch]), kArgmaxThreads, 0, s>>>(
+      logits, vocab, am);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_walk(token, parent, am, n, vocab, prefix, m, path, out_tokens, new_pos,
-                     new_parent, n_survivors, dev_status, s);
+  return launch_walk_batched(token, parent, am, batch, node_offset, vocab, prefix, m, path,
+                             out_tokens, new_pos, new_parent, n_survivors, dev_status, s);
 }
 
 cudaError_t launch_walk(const int32_t* token, const int32_t* parent, const int32_t* am,
                         int32_t n, int32_t vocab, int32_t prefix, int32_t* m, int32_t* path,
                         int32_t* out_tokens, int32_t* new_pos, int32_t* new_parent,
                         int32_t* n_survivors, int32_t* dev_status, cudaStream_t s) {
-  walk_kernel<<<1, 32, 0, s>>>(token, parent, am, n, vocab, prefix, m, path, out_tokens,
-                               new_pos, new_parent, n_survivors, dev_status);
+  const int32_t off[2] = {0, n};
+  return launch_walk_batched(token, parent, am, 1, off, vocab, &prefix, m, path, out_tokens,
+                             new_pos, new_parent, n_survivors, dev_status, s);
+}
+
+cudaError_t launch_walk_batched(const int32_t* token, const int32_t* parent, const int32_t* am,
+                                int32_t batch, const int32_t* node_offset, int32_t vocab,
+                                const int32_t* prefix, int32_t* m, int32_t* path,
+                                int32_t* out_tokens, int32_t* new_pos, int32_t* new_parent,
+                                int32_t* n_survivors, int32_t* dev_status, cudaStream_t s) {
+  WalkJobs jobs{};
+  for (int b = 0; b < batch; ++b) {
+    jobs.off[b] = node_offset[b];
+    jobs.prefix[b] = prefix[b];
+  }
+  jobs.off[batch] = node_offset[batch];
+  walk_kernel<<<batch, 32, 0, s>>>(jobs, token, parent, am, vocab, m, path, out_tokens, new_pos,
+                                   new_parent, n_survivors, dev_status);
   return cudaGetLastError();
 }
 

@@ -61,6 +61,33 @@ tv::AttnProblem attn_problem(const void* q, const void* k, const void* v, int64_
   return p;
 }
 
+// Packed per-request node ranges of the batched acceptance: node_offset[0]
+// is 0 and every request holds 1 to TV_MAX_NODES nodes.
+tv_status check_packed(int32_t batch, const int32_t* node_offset, const int32_t* prefix_len) {
+  if (batch < 1 || batch > TV_MAX_BATCH || !node_offset || !prefix_len) return TV_ERR_INVALID_ARG;
+  if (node_offset[0] != 0) return TV_ERR_INVALID_ARG;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t n = (int64_t)node_offset[b + 1] - node_offset[b];
+    if (n < 1 || n > TV_MAX_NODES || prefix_len[b] < 0) return TV_ERR_INVALID_ARG;
+    if ((int64_t)prefix_len[b] + n > INT32_MAX) return TV_ERR_INVALID_ARG;
+  }
+  return TV_OK;
+}
+
+// Checks shared by the batched compactions: every request's tree size,
+// prefix and new_pos.
+tv_status check_compact_requests(int32_t batch, const int32_t* prefix_len,
+                                 const int32_t* n_nodes, const int32_t* const* new_pos) {
+  if (batch < 1 || batch > TV_MAX_BATCH || !prefix_len || !n_nodes || !new_pos)
+    return TV_ERR_INVALID_ARG;
+  for (int b = 0; b < batch; ++b) {
+    if (!new_pos[b] || prefix_len[b] < 0) return TV_ERR_INVALID_ARG;
+    if (n_nodes[b] < 1 || n_nodes[b] > TV_MAX_NODES) return TV_ERR_INVALID_ARG;
+    if ((int64_t)prefix_len[b] + n_nodes[b] > INT32_MAX / 2) return TV_ERR_UNSUPPORTED;
+  }
+  return TV_OK;
+}
+
 // The attention kernel, then the merge of its split partials.
 tv_status run_attention(const tv::AttnProblem& p, const tv::SplitPlan& plan, void* workspace,
                         tv_stream_t stream) {
@@ -333,6 +360,104 @@ tv_status tv_tree_accept(const float* logits, int32_t vocab, const int32_t* toke
   return from_cuda(tv::launch_accept(logits, vocab, token, parent, n_nodes, prefix_len, am, m,
                                      path, out_tokens, new_pos, new_parent, n_survivors,
                                      dev_status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tv_status tv_tree_accept_batched(int32_t batch, const int32_t* node_offset,
+                                 const int32_t* prefix_len, const float* logits, int32_t vocab,
+                                 const int32_t* token, const int32_t* parent, int32_t* am,
+                                 int32_t* m, int32_t* path, int32_t* out_tokens,
+                                 int32_t* new_pos, int32_t* new_parent, int32_t* n_survivors,
+                                 int32_t* dev_status, tv_stream_t stream) {
+  if (!logits || !token || !parent || !am || !m || !path || !out_tokens || !new_pos ||
+      !new_parent || !n_survivors || vocab < 1)
+    return TV_ERR_INVALID_ARG;
+  const tv_status st = check_packed(batch, node_offset, prefix_len);
+  if (st != TV_OK) return st;
+  if ((reinterpret_cast<uintptr_t>(logits) & 3u) != 0) return TV_ERR_INVALID_ARG;
+  return from_cuda(tv::launch_accept_batched(logits, vocab, token, parent, batch, node_offset,
+                                             prefix_len, am, m, path, out_tokens, new_pos,
+                                             new_parent, n_survivors, dev_status,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tv_status tv_tree_accept_tokens_batched(int32_t batch, const int32_t* node_offset,
+                                        const int32_t* prefix_len, const int32_t* target_token,
+                                        int32_t vocab, const int32_t* token,
+                                        const int32_t* parent, int32_t* m, int32_t* path,
+                                        int32_t* out_tokens, int32_t* new_pos,
+                                        int32_t* new_parent, int32_t* n_survivors,
+                                        int32_t* dev_status, tv_stream_t stream) {
+  if (!target_token || !token || !parent || !m || !path || !out_tokens || !new_pos ||
+      !new_parent || !n_survivors || vocab < 1)
+    return TV_ERR_INVALID_ARG;
+  const tv_status st = check_packed(batch, node_offset, prefix_len);
+  if (st != TV_OK) return st;
+  return from_cuda(tv::launch_walk_batched(token, parent, target_token, batch, node_offset,
+                                           vocab, prefix_len, m, path, out_tokens, new_pos,
+                                           new_parent, n_survivors, dev_status,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tv_status tv_kv_compact_batched(int32_t batch, void* const* k_cache, void* const* v_cache,
+                                const int64_t* layer_stride_elems, const int64_t* cap,
+                                const int32_t* prefix_len, const int32_t* n_nodes,
+                                const int32_t* const* new_pos, int32_t n_layers, int32_t hkv,
+                                int32_t d, int32_t dtype, int32_t* dev_status,
+                                tv_stream_t stream) {
+  const int es = elem_size(dtype);
+  if (!k_cache || !v_cache || !layer_stride_elems || !cap || es == 0) return TV_ERR_INVALID_ARG;
+  if (n_layers < 1 || hkv < 1 || d < 1) return TV_ERR_INVALID_ARG;
+  tv_status st = check_compact_requests(batch, prefix_len, n_nodes, new_pos);
+  if (st != TV_OK) return st;
+  const int64_t row_bytes = (int64_t)d * es;
+  if (row_bytes % 16 != 0 || row_bytes > 512) return TV_ERR_UNSUPPORTED;
+  if ((int64_t)n_layers * hkv * 2 > INT32_MAX) return TV_ERR_UNSUPPORTED;
+  int64_t stride_bytes[TV_MAX_BATCH];
+  for (int b = 0; b < batch; ++b) {
+    if (!k_cache[b] || !v_cache[b] || !aligned16(k_cache[b]) || !aligned16(v_cache[b]))
+      return TV_ERR_INVALID_ARG;
+    if (cap[b] < 1) return TV_ERR_INVALID_ARG;
+    if ((int64_t)prefix_len[b] + n_nodes[b] > cap[b]) return TV_ERR_CAPACITY;
+    if (layer_stride_elems[b] < (int64_t)hkv * cap[b] * d) return TV_ERR_INVALID_ARG;
+    stride_bytes[b] = layer_stride_elems[b] * es;
+  }
+  return from_cuda(tv::launch_compact_batched(batch, k_cache, v_cache, stride_bytes, cap,
+                                              nullptr, prefix_len, n_nodes, new_pos, n_layers,
+                                              hkv, (int32_t)row_bytes, 0, 0, dev_status,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tv_status tv_kv_compact_batched_paged(int32_t batch, void* k_pool, void* v_pool,
+                                      int32_t n_layers, int64_t layer_stride_elems,
+                                      int32_t num_pages, int32_t hkv, int32_t page_size,
+                                      int32_t d, int32_t dtype, const int32_t* const* page_table,
+                                      const int32_t* prefix_len, const int32_t* n_nodes,
+                                      const int32_t* const* new_pos, int32_t* dev_status,
+                                      tv_stream_t stream) {
+  const int es = elem_size(dtype);
+  if (!k_pool || !v_pool || !page_table || es == 0) return TV_ERR_INVALID_ARG;
+  if (n_layers < 1 || hkv < 1 || d < 1 || num_pages < 1 || page_size < 1)
+    return TV_ERR_INVALID_ARG;
+  tv_status st = check_compact_requests(batch, prefix_len, n_nodes, new_pos);
+  if (st != TV_OK) return st;
+  const int64_t row_bytes = (int64_t)d * es;
+  if (row_bytes % 16 != 0 || row_bytes > 512) return TV_ERR_UNSUPPORTED;
+  if (!aligned16(k_pool) || !aligned16(v_pool)) return TV_ERR_INVALID_ARG;
+  if (layer_stride_elems < (int64_t)num_pages * hkv * page_size * d) return TV_ERR_INVALID_ARG;
+  if ((int64_t)n_layers * hkv * 2 > INT32_MAX) return TV_ERR_UNSUPPORTED;
+  void* ks[TV_MAX_BATCH];
+  void* vs[TV_MAX_BATCH];
+  int64_t stride_bytes[TV_MAX_BATCH];
+  for (int b = 0; b < batch; ++b) {
+    if (!page_table[b]) return TV_ERR_INVALID_ARG;
+    ks[b] = k_pool;
+    vs[b] = v_pool;
+    stride_bytes[b] = layer_stride_elems * es;
+  }
+  return from_cuda(tv::launch_compact_batched(batch, ks, vs, stride_bytes, nullptr, page_table,
+                                              prefix_len, n_nodes, new_pos, n_layers, hkv,
+                                              (int32_t)row_bytes, page_size, num_pages,
+                                              dev_status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 tv_status tv_tree_accept_tokens(const int32_t* target_token, int32_t vocab, const int32_t* token,

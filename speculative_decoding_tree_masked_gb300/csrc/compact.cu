@@ -10,6 +10,8 @@
 // A paged cache (a pool [pages][hkv][page_size][d] per layer) maps logical
 // row r to row r % page_size of page page_table[r / page_size]; a move whose
 // source or destination page is outside the pool is skipped and reported.
+// Several requests compact in one launch: grid.y indexes the request, each
+// with its own caches (or page table), prefix, tree size and new_pos.
 #include "common.cuh"
 #include "internal.h"
 
@@ -19,22 +21,42 @@ namespace {
 
 constexpr int kCompactThreads = 256;
 
+// One request's compaction.
+struct CompactJob {
+  char* k;                    // layer 0 of the K cache (or K page pool)
+  char* v;
+  long long layer_stride;     // bytes from one layer to the next
+  long long cap;              // rows per head of a contiguous cache
+  const int32_t* new_pos;     // [n]
+  const int32_t* page_table;  // null: contiguous [hkv][cap][row] per layer
+  int prefix;
+  int n;
+};
+
+template <int MAXB>
+struct CompactJobs {
+  CompactJob job[MAXB];
+};
+
+template <int MAXB>
 __global__ void __launch_bounds__(kCompactThreads)
-compact_kernel(char* __restrict__ kc, char* __restrict__ vc, int hkv, long long layer_stride,
-               long long cap, int row_bytes, int prefix, int n,
-               const int32_t* __restrict__ new_pos, const int32_t* __restrict__ page_table,
+compact_kernel(const __grid_constant__ CompactJobs<MAXB> jobs, int hkv, int row_bytes,
                int page_size, int num_pages, int32_t* dev_status) {
   extern __shared__ uint4 buf[];
   __shared__ int src_row[kMaxNodes], dst_row[kMaxNodes];
   __shared__ uint32_t used[kMaskWords];
   __shared__ int count;
+  const CompactJob& job = jobs.job[blockIdx.y];
+  const int prefix = job.prefix, n = job.n;
+  const int32_t* __restrict__ new_pos = job.new_pos;
+  const int32_t* __restrict__ page_table = job.page_table;
   const int tid = threadIdx.x;
   const int slab = blockIdx.x;
   const int which = slab & 1;
   const int g = (slab >> 1) % hkv;
   const int layer = (slab >> 1) / hkv;
-  char* lbase = (which ? vc : kc) + (size_t)layer * layer_stride;
-  char* base = lbase + (size_t)g * cap * row_bytes;
+  char* lbase = (which ? job.v : job.k) + (size_t)layer * job.layer_stride;
+  char* base = lbase + (size_t)g * job.cap * row_bytes;
   // byte offset of logical row r, or -1 when its page is outside the pool
   auto row_at = [&](int r) -> long long {
     if (page_table == nullptr) return (long long)(base - lbase) + (long long)r * row_bytes;
@@ -102,6 +124,27 @@ tree_mask_kernel(const int32_t* __restrict__ parent, int n, uint32_t* __restrict
   }
 }
 
+template <int MAXB>
+cudaError_t launch_jobs(const CompactJobs<MAXB>& jobs, int batch, int32_t layers, int32_t hkv,
+                        int32_t row_bytes, int32_t max_n, int32_t page_size, int32_t num_pages,
+                        int32_t* dev_status, cudaStream_t s) {
+  static bool attr_set[64];  // per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(compact_kernel<MAXB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kMaxNodes * 512);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  const size_t smem = (size_t)max_n * row_bytes;
+  const dim3 grid((unsigned)layers * (unsigned)hkv * 2u, (unsigned)batch);
+  compact_kernel<MAXB><<<grid, kCompactThreads, smem, s>>>(jobs, hkv, row_bytes, page_size,
+                                                           num_pages, dev_status);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_compact(void* k, void* v, int32_t layers, int64_t layer_stride_bytes,
@@ -109,22 +152,29 @@ cudaError_t launch_compact(void* k, void* v, int32_t layers, int64_t layer_strid
                            int32_t n, const int32_t* new_pos, int32_t* dev_status,
                            cudaStream_t s, const int32_t* page_table, int32_t page_size,
                            int32_t num_pages) {
-  const size_t smem = (size_t)n * row_bytes;
-  static bool attr_set[64];  // per device
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kMaxNodes * 512);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  CompactJobs<1> jobs{};
+  jobs.job[0] = CompactJob{static_cast<char*>(k), static_cast<char*>(v), layer_stride_bytes,
+                           cap, new_pos, page_table, prefix, n};
+  return launch_jobs(jobs, 1, layers, hkv, row_bytes, n, page_size, num_pages, dev_status, s);
+}
+
+cudaError_t launch_compact_batched(int32_t batch, void* const* k, void* const* v,
+                                   const int64_t* layer_stride_bytes, const int64_t* cap,
+                                   const int32_t* const* page_table, const int32_t* prefix,
+                                   const int32_t* n, const int32_t* const* new_pos,
+                                   int32_t layers, int32_t hkv, int32_t row_bytes,
+                                   int32_t page_size, int32_t num_pages, int32_t* dev_status,
+                                   cudaStream_t s) {
+  CompactJobs<kMaxBatch> jobs{};
+  int max_n = 0;
+  for (int b = 0; b < batch; ++b) {
+    jobs.job[b] = CompactJob{static_cast<char*>(k[b]), static_cast<char*>(v[b]),
+                             layer_stride_bytes[b], cap ? cap[b] : 0, new_pos[b],
+                             page_table ? page_table[b] : nullptr, prefix[b], n[b]};
+    max_n = n[b] > max_n ? n[b] : max_n;
   }
-  const unsigned grid = (unsigned)layers * (unsigned)hkv * 2u;
-  compact_kernel<<<grid, kCompactThreads, smem, s>>>(
-      static_cast<char*>(k), static_cast<char*>(v), hkv, layer_stride_bytes, cap, row_bytes,
-      prefix, n, new_pos, page_table, page_size, num_pages, dev_status);
-  return cudaGetLastError();
+  return launch_jobs(jobs, batch, layers, hkv, row_bytes, max_n, page_size, num_pages,
+                     dev_status, s);
 }
 
 cudaError_t launch_tree_mask(const int32_t* parent, int32_t n, uint32_t* words,

@@ -92,6 +92,22 @@ cudaError_t launch_accept(const float* logits, int32_t vocab, const int32_t* tok
                           int32_t* new_parent, int32_t* n_survivors, int32_t* dev_status,
                           cudaStream_t s);
 
+// Several requests with packed node arrays: request b owns nodes
+// [node_offset[b], node_offset[b + 1]) (host array of batch + 1 entries) and
+// has prefix length prefix[b] (host); m and n_survivors hold one entry per
+// request and request b's out_tokens start at node_offset[b] + b.
+cudaError_t launch_accept_batched(const float* logits, int32_t vocab, const int32_t* token,
+                                  const int32_t* parent, int32_t batch,
+                                  const int32_t* node_offset, const int32_t* prefix,
+                                  int32_t* am, int32_t* m, int32_t* path, int32_t* out_tokens,
+                                  int32_t* new_pos, int32_t* new_parent, int32_t* n_survivors,
+                                  int32_t* dev_status, cudaStream_t s);
+cudaError_t launch_walk_batched(const int32_t* token, const int32_t* parent, const int32_t* am,
+                                int32_t batch, const int32_t* node_offset, int32_t vocab,
+                                const int32_t* prefix, int32_t* m, int32_t* path,
+                                int32_t* out_tokens, int32_t* new_pos, int32_t* new_parent,
+                                int32_t* n_survivors, int32_t* dev_status, cudaStream_t s);
+
 // Maximum-likelihood expansion: slices of each frontier logits row.
 struct ExpandPlan {
   int chunks;      // slices per row
@@ -127,6 +143,17 @@ cudaError_t launch_compact(void* k, void* v, int32_t layers, int64_t layer_strid
                            int32_t n, const int32_t* new_pos, int32_t* dev_status,
                            cudaStream_t s, const int32_t* page_table = nullptr,
                            int32_t page_size = 0, int32_t num_pages = 0);
+
+// Several requests in one launch: request b's caches k[b], v[b] (layer l at
+// l * layer_stride_bytes[b]), contiguous with cap[b] rows per head, or paged
+// through page_table[b] (cap may then be null).  All arrays are host arrays.
+cudaError_t launch_compact_batched(int32_t batch, void* const* k, void* const* v,
+                                   const int64_t* layer_stride_bytes, const int64_t* cap,
+                                   const int32_t* const* page_table, const int32_t* prefix,
+                                   const int32_t* n, const int32_t* const* new_pos,
+                                   int32_t layers, int32_t hkv, int32_t row_bytes,
+                                   int32_t page_size, int32_t num_pages, int32_t* dev_status,
+                                   cudaStream_t s);
 
 // The target's LM head fused with the argmax (bf16 hidden states and weights).
 size_t lm_head_workspace_bytes(int32_t n, int32_t vocab, int sm_count);

@@ -241,3 +241,66 @@ def test_paged_host_checks(lib):
     assert compact(n=0) == 1
     assert compact(d=12) == 2                   # rows not whole 16-byte vectors
     assert compact(pages=0) == 1
+
+
+def test_batched_accept_and_compaction_host_checks(lib):
+    import ctypes
+    fake = ctypes.c_void_p(0x1000)
+
+    def arr(ctype, vals):
+        return ctypes.cast((ctype * len(vals))(*vals), ctypes.c_void_p)
+
+    def accept(batch=2, off=(0, 5, 12), P=(10, 20), V=100, logits=fake, tokens=False):
+        o, p = arr(ctypes.c_int32, list(off)), arr(ctypes.c_int32, list(P))
+        if tokens:
+            return lib.tv_tree_accept_tokens_batched(batch, o, p, logits, V, fake, fake, fake,
+                                                     fake, fake, fake, fake, fake, None, None)
+        return lib.tv_tree_accept_batched(batch, o, p, logits, V, fake, fake, fake, fake, fake,
+                                          fake, fake, fake, fake, None, None)
+    for tokens in (False, True):
+        assert accept(batch=0, tokens=tokens) == 1
+        assert accept(batch=17, tokens=tokens) == 1
+        assert accept(off=(1, 5, 12), tokens=tokens) == 1          # must start at 0
+        assert accept(off=(0, 5, 5), tokens=tokens) == 1           # an empty request
+        assert accept(off=(0, 5, 140), tokens=tokens) == 1         # 135 nodes > 128
+        assert accept(off=(0, 7, 5), tokens=tokens) == 1           # decreasing
+        assert accept(P=(10, -1), tokens=tokens) == 1
+        assert accept(V=0, tokens=tokens) == 1
+        assert accept(logits=None, tokens=tokens) == 1
+    assert accept(logits=ctypes.c_void_p(0x1002)) == 1             # logits not 4-byte aligned
+    assert lib.tv_tree_accept_batched(2, None, arr(ctypes.c_int32, [0, 0]), fake, 10, fake, fake,
+                                      fake, fake, fake, fake, fake, fake, fake, None, None) == 1
+
+    def compact(batch=2, n=(5, 7), P=(10, 20), cap=(100, 100), stride=None, d=128, dt=1,
+                ptrs=(0x1000, 0x2000), newpos=(0x1000, 0x1000)):
+        stride = stride or [2 * c * d for c in cap]
+        kv = arr(ctypes.c_void_p, list(ptrs))
+        return lib.tv_kv_compact_batched(batch, kv, kv, arr(ctypes.c_int64, list(stride)),
+                                         arr(ctypes.c_int64, list(cap)),
+                                         arr(ctypes.c_int32, list(P)),
+                                         arr(ctypes.c_int32, list(n)),
+                                         arr(ctypes.c_void_p, list(newpos)), 3, 2, d, dt, None,
+                                         None)
+    assert compact(batch=0) == 1
+    assert compact(batch=17) == 1
+    assert compact(n=(5, 0)) == 1
+    assert compact(n=(5, 129)) == 1
+    assert compact(P=(-1, 20)) == 1
+    assert compact(cap=(100, 25)) == 3                            # request 1: 20 + 7 > 25
+    assert compact(stride=(200 * 128, 100)) == 1                  # layers would overlap
+    assert compact(ptrs=(0x1000, 0x2008)) == 1                    # misaligned
+    assert compact(ptrs=(0x1000, 0)) == 1
+    assert compact(newpos=(0x1000, 0)) == 1
+    assert compact(d=6) == 2                                      # 12-byte rows
+    assert compact(dt=7) == 1
+
+    def paged(batch=2, n=(5, 7), P=(10, 20), stride=10 * 2 * 64 * 128, ps=64, tabs=(0x1000, 0x2000)):
+        return lib.tv_kv_compact_batched_paged(
+            batch, fake, fake, 3, stride, 10, 2, ps, 128, 1, arr(ctypes.c_void_p, list(tabs)),
+            arr(ctypes.c_int32, list(P)), arr(ctypes.c_int32, list(n)),
+            arr(ctypes.c_void_p, [0x1000, 0x1000]), None, None)
+    assert paged(batch=0) == 1
+    assert paged(tabs=(0x1000, 0)) == 1
+    assert paged(stride=100) == 1
+    assert paged(ps=0) == 1
+    assert paged(n=(200, 7)) == 1
