@@ -276,46 +276,86 @@ def run_reference(args, rank, world):
 # --------------------------------------------------------------------------
 
 def _end_to_end(args, world, dev, stream, step, q, logits, token, parent, acc, w):
-    """Seconds for args.steps steps through the public API with the step's
-    inputs copied from pinned host memory and its result read back, plus the
-    bytes copied each way per step."""
+    """Seconds for args.steps steps through the public API with every step's
+    inputs copied from pinned host memory and its result read back by the
+    host, under two schedules: pipelined (two input buffers; the next step's
+    inputs are copied on a second stream while the current step runs) and
+    serial (copy, step, read back, one step at a time).  Returns
+    (pipelined_s, serial_s, h2d_bytes, d2h_bytes) per the max over ranks."""
     import torch
     import torch.distributed as dist
     q_h = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
     q_h.copy_(q.cpu())
-    lg_h = torch.from_numpy(w.logits).pin_memory()
-    tk_h = torch.from_numpy(w.token).pin_memory()
-    pr_h = torch.from_numpy(w.parent).pin_memory()
-    q_d, lg_d = torch.empty_like(q), torch.empty_like(logits)
-    tk_d, pr_d = torch.empty_like(token), torch.empty_like(parent)
+    host = (q_h, torch.from_numpy(w.logits).pin_memory(),
+            torch.from_numpy(w.token).pin_memory(), torch.from_numpy(w.parent).pin_memory())
+    slots = [tuple(torch.empty_like(x) for x in (q, logits, token, parent)) for _ in range(2)]
     res_h = {k: torch.empty(acc[k].shape, dtype=torch.int32, pin_memory=True)
              for k in ("m", "out_tokens", "new_pos", "n_survivors")}
-    pairs = ((q_d, q_h), (lg_d, lg_h), (tk_d, tk_h), (pr_d, pr_h))
-    g_e2e = torch.cuda.CUDAGraph()
+    copy_stream = torch.cuda.Stream(dev)
+    graphs = []
     with torch.cuda.stream(stream):
-        for dst, src in pairs:
-            dst.copy_(src, non_blocking=True)
-        step(q_d, lg_d, tk_d, pr_d)
-    torch.cuda.synchronize()
-    with torch.cuda.graph(g_e2e, stream=stream):
-        step(q_d, lg_d, tk_d, pr_d)
-    h2d = sum(src.numel() * src.element_size() for _, src in pairs)
-    d2h = sum(x.numel() * x.element_size() for x in res_h.values())
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for _ in range(args.steps):
-            for dst, src in pairs:
+        for slot in slots:
+            for dst, src in zip(slot, host):
                 dst.copy_(src, non_blocking=True)
-            g_e2e.replay()
+            step(*slot)
+    torch.cuda.synchronize()
+    for slot in slots:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(*slot)
+        graphs.append(g)
+    h2d = sum(src.numel() * src.element_size() for src in host)
+    d2h = sum(x.numel() * x.element_size() for x in res_h.values())
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def upload(slot, s):
+        with torch.cuda.stream(s):
+            for dst, src in zip(slot, host):
+                dst.copy_(src, non_blocking=True)
+
+    def run_and_read(i):
+        with torch.cuda.stream(stream):
+            graphs[i].replay()
             for k, hbuf in res_h.items():
                 hbuf.copy_(acc[k], non_blocking=True)
-            stream.synchronize()
-            _ = int(res_h["m"][0])  # the host reads the result
-    secs = time.perf_counter() - t0
-    return max_over_ranks(secs, world, dev), h2d, d2h
+
+    # serial: every step waits for its own inputs
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        upload(slots[0], stream)
+        run_and_read(0)
+        stream.synchronize()
+        _ = int(res_h["m"][0])  # the host reads the result
+    serial = time.perf_counter() - t0
+
+    # pipelined: slot i % 2 feeds step i; step i + 1's upload overlaps step i
+    copied = [torch.cuda.Event() for _ in range(2)]
+    freed = [torch.cuda.Event() for _ in range(2)]
+    for ev in freed:
+        ev.record(stream)
+    barrier()
+    t0 = time.perf_counter()
+    upload(slots[0], copy_stream)
+    copied[0].record(copy_stream)
+    for i in range(args.steps):
+        s = i & 1
+        stream.wait_event(copied[s])
+        run_and_read(s)
+        freed[s].record(stream)
+        if i + 1 < args.steps:
+            copy_stream.wait_event(freed[1 - s])
+            upload(slots[1 - s], copy_stream)
+            copied[1 - s].record(copy_stream)
+        stream.synchronize()
+        _ = int(res_h["m"][0])
+    pipelined = time.perf_counter() - t0
+    torch.cuda.synchronize()
+    return (max_over_ranks(pipelined, world, dev), max_over_ranks(serial, world, dev), h2d, d2h)
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -462,7 +502,10 @@ def run_gpu(args, rank, world, local_rank):
         "cpu_baseline": cpu,
         "e2e": None if e2e is None else {
             "value": job_throughput(world, NODES, args.steps, e2e[0]), "unit": "tree tokens/s",
-            "h2d_bytes_per_step": e2e[1], "d2h_bytes_per_step": e2e[2]},
+            "h2d_bytes_per_step": e2e[2], "d2h_bytes_per_step": e2e[3],
+            "schedule": "two input buffers: step i+1's inputs are copied on a second stream "
+                        "while step i runs; every step's result is read back by the host",
+            "serial_value": job_throughput(world, NODES, args.steps, e2e[1])},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(peaks["sm_max_mhz"]),
         "verify_steps_per_s": world * 1e3 / ms,
