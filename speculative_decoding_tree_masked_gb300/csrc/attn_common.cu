@@ -25,7 +25,7 @@ constexpr int kTcRowsPerTile = 128;
 constexpr int kTcKeys = 128;      // key block of the tensor-core kernel
 constexpr int kTcCtasPerSm = 1;
 
-int cached_sm[64];
+std::atomic<int> cached_sm[64];  // per device (host threads may race here)
 }  // namespace
 
 // The bf16 tensor-core kernel is switched in once it is built.

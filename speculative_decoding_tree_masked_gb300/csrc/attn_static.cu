@@ -14,7 +14,9 @@ namespace {
 static __device__ __align__(256) unsigned char g_static_scratch[TV_STATIC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices];  // device address of the array, per device
+// device address of the array, per device (host threads may race to fill an
+// entry; every racer stores the same address)
+std::atomic<void*> g_scratch_addr[kMaxDevices];
 
 }  // namespace
 
@@ -29,15 +31,14 @@ tv_status tv_tree_attn_verify_static(const void* q, const void* k_cache, const v
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TV_ERR_CUDA;
   const size_t need = tv_attn_workspace_size(n_nodes, hq, hkv, d, dtype, prefix_len);
   if (need > TV_STATIC_SCRATCH_BYTES) return TV_ERR_CAPACITY;
-  if (g_scratch_addr[dev] == nullptr) {
-    void* addr = nullptr;
+  void* addr = g_scratch_addr[dev].load();
+  if (addr == nullptr) {
     if (cudaGetSymbolAddress(&addr, g_static_scratch) != cudaSuccess || addr == nullptr)
       return TV_ERR_CUDA;
-    g_scratch_addr[dev] = addr;
+    g_scratch_addr[dev].store(addr);
   }
   return tv_tree_attn_verify(q, k_cache, v_cache, cap, prefix_len, n_nodes, parent, out, hq, hkv,
-                             d, dtype, scale, g_scratch_addr[dev], TV_STATIC_SCRATCH_BYTES,
-                             dev_status, stream);
+                             d, dtype, scale, addr, TV_STATIC_SCRATCH_BYTES, dev_status, stream);
 }
 
 }  // extern "C"

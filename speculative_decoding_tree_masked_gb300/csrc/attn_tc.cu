@@ -65,15 +65,17 @@
 namespace tv {
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
+  // looked up once; the initialisation of a function-local static is
+  // thread-safe
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* f = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
@@ -845,7 +847,7 @@ bool make_q_map(CUtensorMap* map, const void* base, int d, int n, int hq, int gr
 
 template <int D, int MAXB, bool PAGED>
 cudaError_t set_smem_attr() {
-  static bool attr_set[64];
+  static std::atomic<bool> attr_set[64];  // per device (host threads may race here)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

@@ -128,7 +128,7 @@ template <int MAXB>
 cudaError_t launch_jobs(const CompactJobs<MAXB>& jobs, int batch, int32_t layers, int32_t hkv,
                         int32_t row_bytes, int32_t max_n, int32_t page_size, int32_t num_pages,
                         int32_t* dev_status, cudaStream_t s) {
-  static bool attr_set[64];  // per device
+  static std::atomic<bool> attr_set[64];  // per device (host threads may race here)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

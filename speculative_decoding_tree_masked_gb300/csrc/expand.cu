@@ -577,7 +577,7 @@ cudaError_t launch_expand(const float* logits, int32_t vocab, int32_t n_frontier
                                                             static_cast<float*>(ws));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  static bool attr_set[64];
+  static std::atomic<bool> attr_set[64];  // per device (host threads may race here)
   int dev = 0;
   e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

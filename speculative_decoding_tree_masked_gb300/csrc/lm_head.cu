@@ -378,7 +378,7 @@ bool make_rows_map(CUtensorMap* map, const void* base, int d, long long rows, in
 
 template <int NC>
 cudaError_t launch_nc(const LmArgs& args, int grid, int smem, cudaStream_t s) {
-  static bool attr_set[64];
+  static std::atomic<bool> attr_set[64];  // per device (host threads may race here)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
