@@ -458,6 +458,23 @@ TV_API tv_status tv_tree_accept_tokens_batched(int32_t batch, const int32_t* nod
                                                int32_t* n_survivors, int32_t* dev_status,
                                                tv_stream_t stream);
 
+/* tv_tree_accept_sampled over packed requests: temperature (float), seed
+ * and offset (uint64) are HOST arrays of `batch` entries, one sampling
+ * setting per request; node i of request b draws with the counter of its
+ * index within the request, (i, offset[b], 0, 0), under key (seed[b], 0),
+ * so every request's draws equal those of tv_tree_accept_sampled with its
+ * own setting.  sampled is packed like token.  Host-side errors as
+ * tv_tree_accept_sampled and tv_tree_accept_batched. */
+TV_API tv_status tv_tree_accept_sampled_batched(int32_t batch, const int32_t* node_offset,
+                                                const int32_t* prefix_len, const float* logits,
+                                                int32_t vocab, const int32_t* token,
+                                                const int32_t* parent, const float* temperature,
+                                                const uint64_t* seed, const uint64_t* offset,
+                                                int32_t* sampled, int32_t* m, int32_t* path,
+                                                int32_t* out_tokens, int32_t* new_pos,
+                                                int32_t* new_parent, int32_t* n_survivors,
+                                                int32_t* dev_status, tv_stream_t stream);
+
 /*
  * tv_kv_compact for `batch` requests in one launch.  HOST arrays of `batch`
  * entries:

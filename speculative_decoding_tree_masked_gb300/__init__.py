@@ -469,6 +469,42 @@ def tree_accept_tokens_batched(target_token: torch.Tensor, vocab: int, token: to
     return outs
 
 
+def tree_accept_sampled_batched(logits: torch.Tensor, token: torch.Tensor, parent: torch.Tensor,
+                                n_nodes, prefix_lens, temperatures, seeds, offsets,
+                                outs: Optional[dict] = None,
+                                status: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """tree_accept_sampled over packed requests (the layout of
+    tree_accept_batched), each with its own temperature, seed and offset.
+    Returns tree_accept_batched's dict with "sampled" [total] in place of
+    "am"."""
+    _need_cuda(logits, token, parent)
+    total, vocab = logits.shape
+    off = _check_packed(n_nodes, prefix_lens, token, parent)
+    if logits.dtype != torch.float32 or off[-1] != total:
+        raise ValueError("logits must be float32 [sum(n_nodes)][V]")
+    batch = len(n_nodes)
+    if not (len(temperatures) == len(seeds) == len(offsets) == batch):
+        raise ValueError("one temperature, seed and offset per request")
+    if outs is None:
+        outs = _packed_outs(("sampled", "m", "path", "out_tokens", "new_pos", "new_parent",
+                             "n_survivors"), n_nodes, logits.device)
+    mask = 2**64 - 1
+    arrs = [_host_array(ctypes.c_int32, off),
+            _host_array(ctypes.c_int32, [int(x) for x in prefix_lens]),
+            _host_array(ctypes.c_float, [float(t) for t in temperatures]),
+            _host_array(ctypes.c_uint64, [int(x) & mask for x in seeds]),
+            _host_array(ctypes.c_uint64, [int(x) & mask for x in offsets])]
+    cp = [ctypes.cast(a, ctypes.c_void_p) for a in arrs]
+    _check(lib().tv_tree_accept_sampled_batched(
+        batch, cp[0], cp[1], _ptr(logits), vocab, _ptr(token), _ptr(parent), cp[2], cp[3],
+        cp[4], _ptr(outs["sampled"]), _ptr(outs["m"]), _ptr(outs["path"]),
+        _ptr(outs["out_tokens"]), _ptr(outs["new_pos"]), _ptr(outs["new_parent"]),
+        _ptr(outs["n_survivors"]), _ptr(status), _stream(stream, logits.device)),
+        "tv_tree_accept_sampled_batched")
+    outs["node_offset"] = off
+    return outs
+
+
 def batched_request(outs: dict, b: int) -> dict:
     """Request b's results from a packed batched-acceptance dict, as views
     shaped like tree_accept's."""

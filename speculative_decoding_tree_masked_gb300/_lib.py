@@ -56,6 +56,9 @@ SIGNATURES = {
     "tv_tree_accept_tokens_batched": (c_i32, [c_i32, c_ptr, c_ptr, c_ptr, c_i32, c_ptr, c_ptr,
                                               c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr,
                                               c_ptr]),
+    "tv_tree_accept_sampled_batched": (c_i32, [c_i32, c_ptr, c_ptr, c_ptr, c_i32, c_ptr, c_ptr,
+                                               c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr,
+                                               c_ptr, c_ptr, c_ptr, c_ptr, c_ptr]),
     "tv_kv_compact_batched": (c_i32, [c_i32, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr,
                                       c_i32, c_i32, c_i32, c_i32, c_ptr, c_ptr]),
     "tv_kv_compact_batched_paged": (c_i32, [c_i32, c_ptr, c_ptr, c_i32, c_i64, c_i32, c_i32,

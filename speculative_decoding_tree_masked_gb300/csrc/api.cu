@@ -398,6 +398,29 @@ tv_status tv_tree_accept_tokens_batched(int32_t batch, const int32_t* node_offse
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
+tv_status tv_tree_accept_sampled_batched(int32_t batch, const int32_t* node_offset,
+                                         const int32_t* prefix_len, const float* logits,
+                                         int32_t vocab, const int32_t* token,
+                                         const int32_t* parent, const float* temperature,
+                                         const uint64_t* seed, const uint64_t* offset,
+                                         int32_t* sampled, int32_t* m, int32_t* path,
+                                         int32_t* out_tokens, int32_t* new_pos,
+                                         int32_t* new_parent, int32_t* n_survivors,
+                                         int32_t* dev_status, tv_stream_t stream) {
+  if (!logits || !token || !parent || !temperature || !seed || !offset || !sampled || !m ||
+      !path || !out_tokens || !new_pos || !new_parent || !n_survivors || vocab < 1)
+    return TV_ERR_INVALID_ARG;
+  const tv_status st = check_packed(batch, node_offset, prefix_len);
+  if (st != TV_OK) return st;
+  for (int b = 0; b < batch; ++b)
+    if (!(temperature[b] > 0.f) || std::isinf(temperature[b])) return TV_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(logits) & 3u) != 0) return TV_ERR_INVALID_ARG;
+  return from_cuda(tv::launch_accept_sampled_batched(
+      logits, vocab, token, parent, batch, node_offset, prefix_len, temperature, seed, offset,
+      sampled, m, path, out_tokens, new_pos, new_parent, n_survivors, dev_status,
+      reinterpret_cast<cudaStream_t>(stream)));
+}
+
 tv_status tv_kv_compact_batched(int32_t batch, void* const* k_cache, void* const* v_cache,
                                 const int64_t* layer_stride_elems, const int64_t* cap,
                                 const int32_t* prefix_len, const int32_t* n_nodes,

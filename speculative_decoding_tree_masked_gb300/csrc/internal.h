@@ -138,6 +138,17 @@ cudaError_t launch_accept_sampled(const float* logits, int32_t vocab, const int3
                                   int32_t* sampled, int32_t* m, int32_t* path,
                                   int32_t* out_tokens, int32_t* new_pos, int32_t* new_parent,
                                   int32_t* n_survivors, int32_t* dev_status, cudaStream_t s);
+// Sampling verification over packed requests (host arrays of batch entries:
+// temperature, seed, offset, prefix; node_offset of batch + 1).
+cudaError_t launch_accept_sampled_batched(const float* logits, int32_t vocab,
+                                          const int32_t* token, const int32_t* parent,
+                                          int32_t batch, const int32_t* node_offset,
+                                          const int32_t* prefix, const float* temperature,
+                                          const uint64_t* seed, const uint64_t* offset,
+                                          int32_t* sampled, int32_t* m, int32_t* path,
+                                          int32_t* out_tokens, int32_t* new_pos,
+                                          int32_t* new_parent, int32_t* n_survivors,
+                                          int32_t* dev_status, cudaStream_t s);
 // Contiguous caches [hkv][cap][row] per layer, or (page_table given) page
 // pools [num_pages][hkv][page_size][row] per layer.
 cudaError_t launch_compact(void* k, void* v, int32_t layers, int64_t layer_stride_bytes,

@@ -78,9 +78,20 @@ __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2,
   }
 }
 
+// Draw parameters of a packed batch: rows [off[b], off[b + 1]) are request
+// b's nodes; its node i draws at temperature 1 / inv_t[b] with key
+// (seed[b], 0) and counter (i, offset[b], 0, 0).
+struct SampleJobs {
+  int32_t off[kMaxBatch + 1];
+  int32_t batch;
+  float inv_t[kMaxBatch];
+  uint64_t seed[kMaxBatch];
+  uint64_t offset[kMaxBatch];
+};
+
 __global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kSampleThreads)
-sample_kernel(const float* __restrict__ logits, int vocab, float inv_t, uint64_t seed,
-              uint64_t offset, int32_t* __restrict__ sampled) {
+sample_kernel(const float* __restrict__ logits, int vocab, const __grid_constant__ SampleJobs jobs,
+              int32_t* __restrict__ sampled) {
   __shared__ float w_m[kSampleWarps], w_s[kSampleWarps];
   __shared__ double w_mass[kSampleWarps];  // each warp's run's mass at the row maximum
   __shared__ float cta_m;                  // this CTA's maximum, read by the cluster
@@ -89,9 +100,11 @@ sample_kernel(const float* __restrict__ logits, int vocab, float inv_t, uint64_t
   __shared__ int sel_owner, sel_warp;      // the drawing CTA and warp (-1: none)
   __shared__ double sel_rem;               // the target mass left inside that warp's run
   cg::cluster_group cluster = cg::this_cluster();
-  const float c = inv_t * 1.4426950408889634f;  // log2(e) / T
-  const int rank = (int)cluster.block_rank();
   const int row = blockIdx.y;
+  int job = 0;  // the request owning this row
+  while (job + 1 < jobs.batch && row >= jobs.off[job + 1]) ++job;
+  const float c = jobs.inv_t[job] * 1.4426950408889634f;  // log2(e) / T
+  const int rank = (int)cluster.block_rank();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int chunk = ((vocab + kSampleCluster * 4 - 1) / (kSampleCluster * 4)) * 4;
   const int beg = min(vocab, rank * chunk);
@@ -190,7 +203,8 @@ sample_kernel(const float* __restrict__ logits, int vocab, float inv_t, uint64_t
       mass[r] = *cluster.map_shared_rank(&cta_s, r);
       S += mass[r];
     }
-    const uint64_t x0 = philox4x64_10_x0((uint64_t)row, offset, 0ull, 0ull, seed, 0ull);
+    const uint64_t x0 = philox4x64_10_x0((uint64_t)(row - jobs.off[job]), jobs.offset[job], 0ull,
+                                         0ull, jobs.seed[job], 0ull);
     const double u = ((double)(x0 >> 11) + 0.5) * (1.0 / 9007199254740992.0);  // 2^-53
     const double t = u * S;
     int owner = -1, last = -1;
@@ -284,13 +298,36 @@ cudaError_t launch_accept_sampled(const float* logits, int32_t vocab, const int3
                                   int32_t* sampled, int32_t* m, int32_t* path,
                                   int32_t* out_tokens, int32_t* new_pos, int32_t* new_parent,
                                   int32_t* n_survivors, int32_t* dev_status, cudaStream_t s) {
-  sample_kernel<<<dim3(kSampleCluster, n), kSampleThreads, 0, s>>>(logits, vocab,
-                                                                   1.0f / temperature, seed,
-                                                                   offset, sampled);
+  const int32_t off[2] = {0, n};
+  return launch_accept_sampled_batched(logits, vocab, token, parent, 1, off, &prefix,
+                                       &temperature, &seed, &offset, sampled, m, path, out_tokens,
+                                       new_pos, new_parent, n_survivors, dev_status, s);
+}
+
+cudaError_t launch_accept_sampled_batched(const float* logits, int32_t vocab,
+                                          const int32_t* token, const int32_t* parent,
+                                          int32_t batch, const int32_t* node_offset,
+                                          const int32_t* prefix, const float* temperature,
+                                          const uint64_t* seed, const uint64_t* offset,
+                                          int32_t* sampled, int32_t* m, int32_t* path,
+                                          int32_t* out_tokens, int32_t* new_pos,
+                                          int32_t* new_parent, int32_t* n_survivors,
+                                          int32_t* dev_status, cudaStream_t s) {
+  SampleJobs jobs{};
+  jobs.batch = batch;
+  for (int b = 0; b < batch; ++b) {
+    jobs.off[b] = node_offset[b];
+    jobs.inv_t[b] = 1.0f / temperature[b];
+    jobs.seed[b] = seed[b];
+    jobs.offset[b] = offset[b];
+  }
+  jobs.off[batch] = node_offset[batch];
+  sample_kernel<<<dim3(kSampleCluster, node_offset[batch]), kSampleThreads, 0, s>>>(
+      logits, vocab, jobs, sampled);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_walk(token, parent, sampled, n, vocab, prefix, m, path, out_tokens, new_pos,
-                     new_parent, n_survivors, dev_status, s);
+  return launch_walk_batched(token, parent, sampled, batch, node_offset, vocab, prefix, m, path,
+                             out_tokens, new_pos, new_parent, n_survivors, dev_status, s);
 }
 
 }  // namespace tv

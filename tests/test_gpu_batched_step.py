@@ -123,6 +123,52 @@ def test_bad_request_is_reported_and_isolated():
         _assert_request(res, b, oracle.tree_accept(lg, tok, par, P))
 
 
+@pytest.mark.parametrize("seed", range(3))
+def test_batched_sampling_equals_single_calls_and_oracle(seed):
+    # every request has its own temperature, seed and offset; its draws and
+    # walk must be exactly those of the single-request call with them, and
+    # the draws the oracle's wherever the uniform is not within 1e-5 of a
+    # cumulative-probability boundary
+    rng = np.random.default_rng(70 + seed)
+    ns = [[64, 1, 17], [int(x) for x in rng.integers(1, 129, 16)], [128, 64]][seed]
+    vocab = [128256, 1000, 33][seed]
+    reqs = []
+    for n in ns:
+        parent = np.asarray(synth.uniform_parent_tree(rng, n, max_depth=8, max_fanout=8),
+                            dtype=np.int32)
+        token = rng.integers(0, vocab, size=n).astype(np.int32)
+        logits = (rng.standard_normal((n, vocab)) * 3).astype(np.float32)
+        reqs.append((parent, token, logits, int(rng.integers(0, 5000))))
+    temps = [float(t) for t in rng.uniform(0.3, 2.0, len(ns))]
+    seeds = [int(x) for x in rng.integers(0, 2**63, len(ns))]
+    offs = [int(x) for x in rng.integers(0, 1000, len(ns))]
+    parent, token, logits = _packed(reqs)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    res = tvp.tree_accept_sampled_batched(logits, token, parent, ns, [r[3] for r in reqs], temps,
+                                          seeds, offs, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for b, (par, tok, lg, P) in enumerate(reqs):
+        one = tvp.tree_accept_sampled(torch.from_numpy(lg).to(DEV), torch.from_numpy(tok).to(DEV),
+                                      torch.from_numpy(par).to(DEV), P, temps[b], seeds[b],
+                                      offs[b])
+        got = tvp.batched_request(res, b)
+        torch.cuda.synchronize()
+        for key in ("sampled", "m", "path", "out_tokens", "new_pos", "new_parent",
+                    "n_survivors"):
+            assert torch.equal(got[key], one[key]), (b, key)
+        s = got["sampled"].cpu().numpy()
+        p = oracle.target_probs(lg.astype(np.float64), temps[b])
+        for i in range(len(par)):
+            u = oracle.node_uniform(seeds[b], offs[b], i)
+            want = oracle.draw_by_inversion(p[i], u)
+            g = int(s[i])
+            if g != want:
+                c = np.cumsum(p[i])
+                lo = c[g - 1] if g > 0 else 0.0
+                assert lo - 1e-5 <= u < c[g] + 1e-5, (b, i, g, want)
+
+
 def _bits(t):
     return t.view(torch.int16 if t.element_size() == 2 else torch.int32).cpu().numpy()
 

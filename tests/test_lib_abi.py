@@ -268,6 +268,19 @@ def test_batched_accept_and_compaction_host_checks(lib):
         assert accept(V=0, tokens=tokens) == 1
         assert accept(logits=None, tokens=tokens) == 1
     assert accept(logits=ctypes.c_void_p(0x1002)) == 1             # logits not 4-byte aligned
+
+    def sampled(batch=2, off=(0, 5, 12), T=(1.0, 0.5)):
+        o, p = arr(ctypes.c_int32, list(off)), arr(ctypes.c_int32, [10, 20])
+        t = arr(ctypes.c_float, list(T))
+        u = arr(ctypes.c_uint64, [1, 2])
+        return lib.tv_tree_accept_sampled_batched(batch, o, p, fake, 100, fake, fake, t, u, u,
+                                                  fake, fake, fake, fake, fake, fake, fake, None,
+                                                  None)
+    assert sampled(batch=0) == 1
+    assert sampled(off=(0, 5, 140)) == 1
+    assert sampled(T=(1.0, 0.0)) == 1                             # temperature must be > 0
+    assert sampled(T=(float("inf"), 1.0)) == 1
+    assert sampled(T=(float("nan"), 1.0)) == 1
     assert lib.tv_tree_accept_batched(2, None, arr(ctypes.c_int32, [0, 0]), fake, 10, fake, fake,
                                       fake, fake, fake, fake, fake, fake, fake, None, None) == 1
 
