@@ -203,17 +203,92 @@ def oracle_sample(nodes: int, layers: int, seed: int = 0) -> dict:
                       f"layers; scaled to one full step", "threads": 1, "m": int(res["m"])}
 
 
+def _oracle_worker(seed, layers, items, barrier, results):
+    """One process of the all-cores oracle sample: builds its layers' inputs,
+    waits until every worker is ready, then times the oracle's attention on
+    its (layer, node) items."""
+    import oracle
+    from workloads import synth
+    w = synth.make_workload(WORKLOAD, seed=seed, layers=layers)
+    by_layer = {}
+    for layer, node in items:
+        by_layer.setdefault(layer, []).append(node)
+    inputs = {}
+    for layer in by_layer:
+        q, k, v = synth.make_qkv(w, layer=layer)
+        inputs[layer] = (q.float().numpy(), k.float().numpy(), v.float().numpy())
+    barrier.wait(timeout=600)
+    t0 = time.perf_counter()
+    for layer, nodes in by_layer.items():
+        qn, kn, vn = inputs[layer]
+        oracle.tree_attention(qn, kn, vn, w.prefix, w.parent, nodes=nodes)
+    results.put(time.perf_counter() - t0)
+
+
+def oracle_sample_all_cores(nodes: int, layers: int, workers: int, seed: int = 0) -> dict:
+    """oracle_sample with the attention of the sampled (layer, node) items
+    dealt round-robin to `workers` processes running at once (one BLAS
+    thread each); acceptance and compaction run in this process, as in
+    oracle_sample.  The attention time is the slowest worker's."""
+    import multiprocessing as mp
+
+    import oracle
+    from workloads import synth
+    w = synth.make_workload(WORKLOAD, seed=seed, layers=layers)
+    t0 = time.perf_counter()
+    res = oracle.tree_accept(w.logits, w.token, w.parent, w.prefix)
+    t_acc = time.perf_counter() - t0
+    t_comp = 0.0
+    for layer in range(layers):
+        _, k, v = synth.make_qkv(w, layer=layer)
+        kb, vb = k.view(torch_int16()).numpy(), v.view(torch_int16()).numpy()
+        t0 = time.perf_counter()
+        oracle.kv_compact(kb, w.prefix, res["new_pos"])
+        oracle.kv_compact(vb, w.prefix, res["new_pos"])
+        t_comp += time.perf_counter() - t0
+    sample_nodes = list(range(0, NODES, max(1, NODES // nodes)))[:nodes]
+    items = [(layer, node) for layer in range(layers) for node in sample_nodes]
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(workers)
+    results = ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker, args=(seed, layers, items[k::workers], barrier,
+                                                      results))
+             for k in range(workers)]
+    for p in procs:
+        p.start()
+    try:
+        times = [results.get(timeout=900) for _ in procs]
+    finally:
+        for p in procs:
+            p.join(timeout=60)
+            if p.is_alive():
+                p.terminate()
+    if any(p.exitcode != 0 for p in procs):
+        raise RuntimeError("an oracle worker failed")
+    t_attn = max(times)
+    t_step = t_attn * (NODES * LAYERS) / len(items) + t_acc + (t_comp / layers) * LAYERS
+    return {"t_step_s": t_step, "sample_s": sum(times) + t_acc + t_comp,
+            "sample": f"attention of {len(sample_nodes)} of {NODES} tree nodes x {layers} of "
+                      f"{LAYERS} layers over {workers} processes, full acceptance, compaction "
+                      f"of {layers} of {LAYERS} layers; scaled to one full step",
+            "threads": workers, "m": int(res["m"])}
+
+
 def torch_int16():
     import torch
     return torch.int16
 
 
-def _oracle_subprocess(nodes, layers, repeats):
+def _oracle_subprocess(nodes, layers, repeats, workers=0):
+    """oracle_sample (workers 0) or oracle_sample_all_cores in a fresh CPU-only
+    process with one BLAS thread per process."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
-            "print(json.dumps([bench.oracle_sample(%d, %d, seed=r) for r in range(%d)]))"
-            % (ROOT, nodes, layers, repeats))
+    call = ("bench.oracle_sample(%d, %d, seed=r)" % (nodes, layers) if workers == 0 else
+            "bench.oracle_sample_all_cores(%d, %d, %d, seed=r)" % (nodes, layers, workers))
+    code = ("import json, sys; sys.path.insert(0, %r); import bench\n"
+            "if __name__ == '__main__':\n"
+            "    print(json.dumps([%s for r in range(%d)]))" % (ROOT, call, repeats))
     out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                          timeout=1800)
     if out.returncode != 0:
@@ -487,8 +562,16 @@ def run_gpu(args, rank, world, local_rank):
         cpu = None
     else:
         s = _oracle_subprocess(64, 2, 1)[0]
-        cpu = {"value": NODES / s["t_step_s"], "unit": "tree tokens/s", "cores": 1,
+        one = {"value": NODES / s["t_step_s"], "unit": "tree tokens/s", "cores": 1,
                "kind": "oracle", "sample": s["sample"], "sample_seconds": s["sample_s"]}
+        workers = os.cpu_count() or 1
+        try:
+            a = _oracle_subprocess(64, 4, 1, workers=workers)[0]
+            cpu = {"value": NODES / a["t_step_s"], "unit": "tree tokens/s", "cores": workers,
+                   "kind": "oracle", "sample": a["sample"], "sample_seconds": a["sample_s"],
+                   "one_thread": one}
+        except Exception as e:  # the 1-thread figure stands alone
+            cpu = dict(one, all_cores_error=str(e)[-300:])
 
     ms = total_ms / args.steps
     line = _line_base(args, world)
