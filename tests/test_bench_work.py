@@ -62,3 +62,12 @@ def test_reference_arm_prints_the_contract_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert "workload" in d["config"]
+
+
+def test_all_cores_oracle_sample_runs_and_scales():
+    # the cpu_baseline leg's parallel sample, small: 2 processes, 4 nodes of one layer
+    s = bench._oracle_subprocess(4, 1, 1, workers=2)[0]
+    one = bench._oracle_subprocess(4, 1, 1)[0]
+    assert s["threads"] == 2 and "over 2 processes" in s["sample"]
+    assert s["t_step_s"] > 0 and one["t_step_s"] > 0
+    assert s["m"] == one["m"]                       # the same acceptance on the same inputs
