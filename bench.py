@@ -564,7 +564,8 @@ def run_gpu(args, rank, world, local_rank):
         s = _oracle_subprocess(64, 2, 1)[0]
         one = {"value": NODES / s["t_step_s"], "unit": "tree tokens/s", "cores": 1,
                "kind": "oracle", "sample": s["sample"], "sample_seconds": s["sample_s"]}
-        workers = os.cpu_count() or 1
+        workers = (len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+                   else os.cpu_count()) or 1
         try:
             a = _oracle_subprocess(64, 4, 1, workers=workers)[0]
             cpu = {"value": NODES / a["t_step_s"], "unit": "tree tokens/s", "cores": workers,
