@@ -10,6 +10,13 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+    config.addinivalue_line("markers", "full_size: runs the benchmark's full-size workload "
+                            "(collected last, so that a run stopping at its first failure has "
+                            "run every smaller test first)")
+
+
+def pytest_collection_modifyitems(config, items):
+    items.sort(key=lambda item: item.get_closest_marker("full_size") is not None)
 
 
 @pytest.fixture(scope="session")
