@@ -1140,12 +1140,9 @@ def _splits_for(tvp, n, hq, hkv, d, prefix):
 
 
 def _attn_splits(tvp):
-    """Split count the library plans for this workload, read off the
-    workspace size: per split, a 4-byte log-sum-exp and a d-wide fp16
-    partial for each of the n * hq rows (plus padding below 512 bytes)."""
-    rows = NODES * HQ
-    nbytes = tvp.attn_workspace_size(NODES, HQ, HKV, D, __import__("torch").bfloat16, PREFIX)
-    return max(1, nbytes // (rows * (2 * D + 4)))
+    """Split count the library plans for this workload on the current GPU."""
+    import torch
+    return tvp.attn_plan(NODES, HQ, HKV, D, torch.bfloat16, PREFIX)["splits"]
 
 
 def main():

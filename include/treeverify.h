@@ -117,6 +117,28 @@ TV_API size_t tv_attn_workspace_size(int32_t n_nodes, int32_t hq, int32_t hkv, i
 TV_API int32_t tv_attn_uses_tensor_cores(int32_t dtype);
 
 /*
+ * tv_attn_plan -- the split plan tv_tree_attn_verify uses for this shape on
+ * a GPU with sm_count SMs (0: the current device's).  Host only: it
+ * launches nothing and, given sm_count > 0, makes no CUDA call.
+ *
+ *   row_groups      CTAs per KV head along the query rows (each CTA holds up
+ *                   to two 128-row tiles on the tensor-core path)
+ *   splits          key splits; the CTAs of one layer are
+ *                   hkv * row_groups * splits, and a combine launch follows
+ *                   when splits > 1
+ *   keys_per_split  keys of every split but the last (a multiple of the key
+ *                   block), the last holding the rest of [0, P + N)
+ *   ws_bytes        workspace bytes (tv_attn_workspace_size gives the same
+ *                   on the current device)
+ * Errors: those of tv_attn_workspace_size's shape checks, TV_ERR_INVALID_ARG
+ * for a negative prefix or sm_count or a null output, TV_ERR_CUDA when
+ * sm_count is 0 and no device answers.
+ */
+TV_API tv_status tv_attn_plan(int32_t n_nodes, int32_t hq, int32_t hkv, int32_t d, int32_t dtype,
+                              int32_t prefix_len, int32_t sm_count, int32_t* row_groups,
+                              int32_t* splits, int32_t* keys_per_split, size_t* ws_bytes);
+
+/*
  * tv_tree_attn_verify -- one layer of tree-masked grouped-query attention of
  * the draft tree against the prefix KV cache plus the tree's own KV.
  *

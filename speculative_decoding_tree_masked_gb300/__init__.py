@@ -87,6 +87,20 @@ def attn_workspace_size(n_nodes: int, hq: int, hkv: int, d: int, dtype: torch.dt
     return int(lib().tv_attn_workspace_size(n_nodes, hq, hkv, d, _DTYPES[dtype], max_prefix))
 
 
+def attn_plan(n_nodes: int, hq: int, hkv: int, d: int, dtype: torch.dtype, prefix_len: int,
+              sm_count: int = 0) -> dict:
+    """The split plan of tree_attn_verify for this shape on a GPU with
+    sm_count SMs (0: the current device's): row_groups, splits,
+    keys_per_split and ws_bytes."""
+    rg, sp, kps = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    ws = ctypes.c_size_t()
+    _check(lib().tv_attn_plan(n_nodes, hq, hkv, d, _DTYPES[dtype], prefix_len, sm_count,
+                              ctypes.byref(rg), ctypes.byref(sp), ctypes.byref(kps),
+                              ctypes.byref(ws)), "tv_attn_plan")
+    return {"row_groups": rg.value, "splits": sp.value, "keys_per_split": kps.value,
+            "ws_bytes": ws.value}
+
+
 def attn_workspace(n_nodes: int, hq: int, hkv: int, d: int, dtype: torch.dtype, max_prefix: int,
                    device) -> torch.Tensor:
     """A workspace tensor large enough for every prefix up to max_prefix."""

@@ -23,6 +23,8 @@ SIGNATURES = {
     "tv_tree_mask": (c_i32, [c_ptr, c_i32, c_ptr, c_ptr, c_ptr]),
     "tv_attn_uses_tensor_cores": (c_i32, [c_i32]),
     "tv_attn_workspace_size": (c_size, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32]),
+    "tv_attn_plan": (c_i32, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_ptr, c_ptr, c_ptr,
+                             c_ptr]),
     "tv_tree_attn_verify": (c_i32, [c_ptr, c_ptr, c_ptr, c_i64, c_i32, c_i32, c_ptr, c_ptr,
                                     c_i32, c_i32, c_i32, c_i32, ctypes.c_float, c_ptr, c_size,
                                     c_ptr, c_ptr]),

@@ -140,6 +140,23 @@ size_t tv_attn_workspace_size(int32_t n_nodes, int32_t hq, int32_t hkv, int32_t 
   return tv::plan_attention(n_nodes, hq, hkv, d, dtype, max_prefix, sms).ws_bytes;
 }
 
+tv_status tv_attn_plan(int32_t n_nodes, int32_t hq, int32_t hkv, int32_t d, int32_t dtype,
+                       int32_t prefix_len, int32_t sm_count, int32_t* row_groups,
+                       int32_t* splits, int32_t* keys_per_split, size_t* ws_bytes) {
+  const tv_status st = check_attn_shape(n_nodes, hq, hkv, d, dtype);
+  if (st != TV_OK) return st;
+  if (prefix_len < 0 || sm_count < 0 || !row_groups || !splits || !keys_per_split || !ws_bytes)
+    return TV_ERR_INVALID_ARG;
+  const int sms = sm_count > 0 ? sm_count : tv::device_sm_count();
+  if (sms <= 0) return TV_ERR_CUDA;
+  const tv::SplitPlan plan = tv::plan_attention(n_nodes, hq, hkv, d, dtype, prefix_len, sms);
+  *row_groups = plan.row_tiles;
+  *splits = plan.splits;
+  *keys_per_split = plan.keys_per_split;
+  *ws_bytes = plan.ws_bytes;
+  return TV_OK;
+}
+
 tv_status tv_tree_attn_verify(const void* q, const void* k_cache, const void* v_cache,
                               int64_t cap, int32_t prefix_len, int32_t n_nodes,
                               const int32_t* parent, void* out, int32_t hq, int32_t hkv,

@@ -317,3 +317,42 @@ def test_batched_accept_and_compaction_host_checks(lib):
     assert paged(stride=100) == 1
     assert paged(ps=0) == 1
     assert paged(n=(200, 7)) == 1
+
+
+def test_attention_plan_is_host_only_and_consistent(lib):
+    import itertools
+
+    import torch
+
+    import speculative_decoding_tree_masked_gb300 as tvp
+    # the full verify step's layer on GB300's 152 SMs: two row groups of two
+    # 128-row tiles per KV head, 9 splits of 4 key blocks (the last holds the
+    # tree block), fp16 partials
+    assert tvp.attn_plan(64, 64, 8, 128, torch.bfloat16, 4096, sm_count=152) == {
+        "row_groups": 2, "splits": 9, "keys_per_split": 512,
+        "ws_bytes": 9 * 4096 * 4 + 9 * 4096 * 128 * 2}
+    shapes = [(64, 8), (32, 8), (4, 1), (7, 1)]
+    for (hq, hkv), n, d, P, sms in itertools.product(shapes, (1, 8, 33, 64, 128), (64, 128),
+                                                     (0, 1, 127, 1024, 4096, 32768, 100000),
+                                                     (1, 8, 152, 256)):
+        p = tvp.attn_plan(n, hq, hkv, d, torch.bfloat16, P, sm_count=sms)
+        keys = P + n
+        assert p["keys_per_split"] % 128 == 0
+        assert (p["splits"] - 1) * p["keys_per_split"] < keys <= p["splits"] * p["keys_per_split"]
+        tiles = -(-(hq // hkv) * n // 128)
+        assert p["row_groups"] == (1 if tiles <= 1 else (tiles + 1) // 2)
+        units = hkv * p["row_groups"]
+        assert units * p["splits"] <= max(sms, units)        # one wave of one-CTA-per-SM
+        if sms == 256:                                       # the no-device workspace bound
+            assert p["ws_bytes"] == tvp.attn_workspace_size(n, hq, hkv, d, torch.bfloat16, P)
+        f = tvp.attn_plan(n, hq, hkv, d, torch.float32, P, sm_count=sms)
+        assert (f["splits"] - 1) * f["keys_per_split"] < keys <= f["splits"] * f["keys_per_split"]
+    import ctypes
+    out = [ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()]
+    refs = [ctypes.byref(x) for x in out]
+    assert lib.tv_attn_plan(64, 64, 8, 96, 1, 4096, 152, *refs) == 2       # d unsupported
+    assert lib.tv_attn_plan(64, 64, 8, 128, 1, -1, 152, *refs) == 1
+    assert lib.tv_attn_plan(64, 64, 8, 128, 1, 4096, -1, *refs) == 1
+    assert lib.tv_attn_plan(64, 64, 8, 128, 1, 4096, 152, None, *refs[1:]) == 1
+    if not torch.cuda.is_available():
+        assert lib.tv_attn_plan(64, 64, 8, 128, 1, 4096, 0, *refs) == 4  # no device to ask
