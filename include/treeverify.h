@@ -20,8 +20,10 @@
  * Conventions shared by every call:
  *   - Every pointer named "device" is CUDA device memory owned by the caller.
  *     The library allocates nothing (the caller passes the workspace) and keeps
- *     no state between calls other than a per-device cache of the SM count and
- *     of driver entry points.
+ *     no state between calls other than per-device caches (the SM count, the
+ *     kernels' shared-memory limits once set, the address of the static
+ *     scratch array) and the driver's tensor-map entry point; host threads
+ *     may call it concurrently.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream) and never synchronises the host.
  *   - Problems visible on the host are returned at once, before anything is
