@@ -66,7 +66,8 @@ typedef enum {
   TV_ERR_CAPACITY = 3,
   TV_ERR_CUDA = 4,
   TV_ERR_INVALID_TREE = 5,
-  TV_ERR_TIMEOUT = 6
+  TV_ERR_TIMEOUT = 6,
+  TV_ERR_BOUNDS = 7  /* a device bounds check failed (checked builds only) */
 } tv_status;
 
 typedef enum {
@@ -81,6 +82,17 @@ TV_API const char* tv_status_string(int32_t status);
 
 /* Library version as 10000*major + 100*minor + patch. */
 TV_API int32_t tv_version(void);
+
+/*
+ * 1 if this library is a checked build, 0 otherwise.  A checked build
+ * (compiled with -DTV_CHECKED=1) tests, in device code, the index ranges of
+ * the accesses that depend on device data or on the launch arithmetic (tree
+ * arrays, compaction rows, partial and output rows) before making them; a
+ * failed test stores TV_ERR_BOUNDS into dev_status (when it is still 0) and
+ * skips that access.  Nothing traps.  It stands in for a memory checker
+ * where none can run.  Normal builds compile the tests away.
+ */
+TV_API int32_t tv_checked_build(void);
 
 /*
  * tv_tree_mask -- the ancestor mask of a draft tree as per-node bitmasks.
@@ -200,9 +212,17 @@ TV_API tv_status tv_tree_attn_verify(const void* q, const void* k_cache, const v
  * and calls no allocating routine.  Arguments, layouts and results are those
  * of tv_tree_attn_verify (minus workspace and ws_bytes).
  *
- *   - The first call on a device looks up the array's device address on that
- *     device (with that device current); make that first call before any
- *     stream capture.  Later calls reuse the cached address.
+ *   - CUDA loads a library's device code and data lazily by default, so the
+ *     16 MiB are reserved on a device at the first call there, not when the
+ *     library is loaded.  Make that first call early: before a framework's
+ *     caching allocator has taken the GPU's free memory (else the first call
+ *     fails with TV_ERR_CUDA), and before any stream capture.
+ *   - Every call made outside a stream capture looks the array's device
+ *     address up again on the current device (a lookup, no allocation), so a
+ *     device reset or a new primary context between calls is harmless.  A
+ *     call made while its stream is being captured reuses the address the
+ *     last uncaptured call on that device found, and fails with TV_ERR_CUDA
+ *     if there was none.
  *   - A problem that needs more scratch than the array holds is rejected with
  *     TV_ERR_CAPACITY before anything is launched (tv_attn_workspace_size
  *     gives the bytes a problem needs).

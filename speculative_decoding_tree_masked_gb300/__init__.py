@@ -23,7 +23,7 @@ import torch
 from . import _lib
 
 TV_OK, TV_ERR_INVALID_ARG, TV_ERR_UNSUPPORTED, TV_ERR_CAPACITY, TV_ERR_CUDA, \
-    TV_ERR_INVALID_TREE, TV_ERR_TIMEOUT = range(7)
+    TV_ERR_INVALID_TREE, TV_ERR_TIMEOUT, TV_ERR_BOUNDS = range(8)
 TV_F32, TV_BF16 = 0, 1
 MAX_NODES = 128
 
@@ -142,9 +142,12 @@ def tree_attn_verify_static(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
                             stream=None) -> torch.Tensor:
     """tree_attn_verify for callers that cannot allocate device memory: no
     workspace is passed or allocated (the library's fixed 16 MiB device
-    scratch array holds the split partials) and `out` must be given.  Make
-    the first call on a device before any stream capture; calls that overlap
-    on the GPU share the scratch array and race."""
+    scratch array holds the split partials) and `out` must be given.
+
+    CUDA loads the array lazily, so its 16 MiB are reserved on a device at
+    the first call there: make that call before a framework's caching
+    allocator takes the GPU's free memory, and before any stream capture.
+    Calls that overlap on the GPU share the scratch array and race."""
     _need_cuda(q, k_cache, v_cache, parent, out)
     n, hq, d = q.shape
     hkv, cap, dk = k_cache.shape

@@ -45,17 +45,22 @@ def _stamp(paths, flags) -> str:
     return h.hexdigest()
 
 
-def build(verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile and link the library; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, extra_flags: list[str] | None = None, csrc: str = CSRC,
+          build_dir: str = BUILD, lib_path: str = LIB) -> str:
+    """Compile and link the library; returns its path.
+
+    extra_flags are added to every compilation (for example -DTV_CHECKED=1
+    for the checked build); csrc, build_dir and lib_path default to the
+    package's own sources, object folder and library."""
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
-    flags = ARCH + CFLAGS + list(extra_flags or [])
-    headers = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + \
+    flags = ARCH + CFLAGS[:-1] + ["-I" + csrc] + list(extra_flags or [])
+    headers = glob.glob(os.path.join(csrc, "*.cuh")) + glob.glob(os.path.join(csrc, "*.h")) + \
         glob.glob(os.path.join(INCLUDE, "*.h"))
-    sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    sources = sorted(glob.glob(os.path.join(csrc, "*.cu")))
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         stamp_file = obj + ".stamp"
         stamp = _stamp([src] + headers, flags)
         if os.path.exists(obj) and os.path.exists(stamp_file):
@@ -76,13 +81,13 @@ def build(verbose: bool = False, extra_flags: list[str] | None = None) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 2)) as ex:
         objs = list(ex.map(compile_one, sources))
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -20,6 +20,7 @@ c_size = ctypes.c_size_t
 SIGNATURES = {
     "tv_status_string": (ctypes.c_char_p, [c_i32]),
     "tv_version": (c_i32, []),
+    "tv_checked_build": (c_i32, []),
     "tv_tree_mask": (c_i32, [c_ptr, c_i32, c_ptr, c_ptr, c_ptr]),
     "tv_attn_uses_tensor_cores": (c_i32, [c_i32]),
     "tv_attn_workspace_size": (c_size, [c_i32, c_i32, c_i32, c_i32, c_i32, c_i32]),

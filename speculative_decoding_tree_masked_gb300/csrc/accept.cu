@@ -249,13 +249,16 @@ walk_kernel(const __grid_constant__ WalkJobs jobs, const int32_t* __restrict__ t
     new_pos[i] = rk >= 0 ? prefix + rk : -1;
     if (rk > m) {
       const int pp = par[i];
-      new_parent[rk - (m + 1)] = (pp == am_last) ? -1 : rank_of[pp] - (m + 1);
+      if (guard(rk - (m + 1) < n && pp >= 0 && pp < n, dev_status))
+        new_parent[rk - (m + 1)] = (pp == am_last) ? -1 : rank_of[pp] - (m + 1);
     }
     if (i >= r) new_parent[i] = -1;
     path[i] = i <= m ? plist[i] : -1;
   }
-  for (int i = lane; i <= n; i += 32)
+  for (int i = lane; i <= n; i += 32) {
+    if (i < m && !guard(plist[i + 1] >= 0 && plist[i + 1] < n, dev_status)) continue;
     out_tokens[i] = i < m ? tok[plist[i + 1]] : (i == m ? amv[am_last] : -1);
+  }
   if (lane == 0) {
     *m_out = m;
     *n_surv = r;

@@ -113,11 +113,14 @@ const char* tv_status_string(int32_t status) {
     case TV_ERR_CUDA: return "CUDA error";
     case TV_ERR_INVALID_TREE: return "invalid draft tree";
     case TV_ERR_TIMEOUT: return "device wait timed out";
+    case TV_ERR_BOUNDS: return "device bounds check failed";
     default: return "unknown status";
   }
 }
 
-int32_t tv_version(void) { return 100; }
+int32_t tv_version(void) { return 101; }
+
+int32_t tv_checked_build(void) { return TV_CHECKED ? 1 : 0; }
 
 tv_status tv_tree_mask(const int32_t* parent, int32_t n_nodes, uint32_t* mask_words,
                        int32_t* dev_status, tv_stream_t stream) {

@@ -10,7 +10,7 @@
 #include <cmath>
 #include <vector>
 
-#include <cuda_fp16.h>
+#include <cuda_bf16.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -70,7 +70,7 @@ SplitPlan plan_attention(int32_t n, int32_t hq, int32_t hkv, int32_t d, int32_t 
   p.keys_per_split = (int32_t)(per * key_block);
   p.splits = (int32_t)((kblocks + per - 1) / per);
   const size_t rows_all = (size_t)n * hq;
-  const size_t o_elem = tc ? 2 : 4;  // fp16 partials for bf16, fp32 for fp32
+  const size_t o_elem = tc ? 2 : 4;  // bf16 partials for bf16, fp32 for fp32
   p.ws_bytes = (partial_o_offset(p.splits, rows_all) + (size_t)p.splits * rows_all * d * o_elem +
                 255) & ~size_t(255);
   return p;
@@ -126,15 +126,15 @@ __device__ __forceinline__ void load_partial(const float* p, float (&o)[2]) {
   const float2 x = *reinterpret_cast<const float2*>(p);
   o[0] = x.x; o[1] = x.y;
 }
-__device__ __forceinline__ void load_partial(const __half* p, float (&o)[4]) {
+// A bf16 value is the top half of the float32 with the same bits.
+__device__ __forceinline__ void load_partial(const __nv_bfloat16* p, float (&o)[4]) {
   const uint2 x = *reinterpret_cast<const uint2*>(p);
-  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&x.x));
-  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&x.y));
-  o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+  o[0] = __uint_as_float(x.x << 16); o[1] = __uint_as_float(x.x & 0xffff0000u);
+  o[2] = __uint_as_float(x.y << 16); o[3] = __uint_as_float(x.y & 0xffff0000u);
 }
-__device__ __forceinline__ void load_partial(const __half* p, float (&o)[2]) {
-  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(p));
-  o[0] = a.x; o[1] = a.y;
+__device__ __forceinline__ void load_partial(const __nv_bfloat16* p, float (&o)[2]) {
+  const uint32_t x = *reinterpret_cast<const uint32_t*>(p);
+  o[0] = __uint_as_float(x << 16); o[1] = __uint_as_float(x & 0xffff0000u);
 }
 
 // One warp per output row: O = sum_s 2^(lse_s - M) O_s / sum_s 2^(lse_s - M).
@@ -220,8 +220,8 @@ cudaError_t launch_combine(const AttnProblem& p, const SplitPlan& plan, const fl
   const auto* w = reinterpret_cast<const uint8_t*>(ws);
   if (p.dtype == TV_BF16) {
     auto* out = static_cast<__nv_bfloat16*>(p.out);
-    if (p.d == 128) launch_combine_d<__half, __nv_bfloat16, 128>(w, plan.splits, rows, out, s);
-    else launch_combine_d<__half, __nv_bfloat16, 64>(w, plan.splits, rows, out, s);
+    if (p.d == 128) launch_combine_d<__nv_bfloat16, __nv_bfloat16, 128>(w, plan.splits, rows, out, s);
+    else launch_combine_d<__nv_bfloat16, __nv_bfloat16, 64>(w, plan.splits, rows, out, s);
   } else {
     // the fp32 path is not latency-critical: one loop kernel
     auto* out = static_cast<float*>(p.out);

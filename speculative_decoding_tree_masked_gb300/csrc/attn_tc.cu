@@ -48,12 +48,12 @@
 // any part of a block past the tree.
 //
 // Every wait is bounded (about two seconds); on expiry the kernel records
-// TV_ERR_TIMEOUT, the other roles stop at their next wait, and the CTA frees
-// its tensor memory and exits.
+// TV_ERR_TIMEOUT and the other roles stop at their next wait.  Before the CTA
+// frees its tensor memory and exits, the producer waits for the copies it
+// requested and the MMA thread for the MMAs it issued, so nothing it started
+// is still writing its shared or tensor memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
-
-#include <cuda_fp16.h>
 
 #include <cmath>
 #include <cstring>
@@ -98,7 +98,7 @@ constexpr uint32_t kSleepHintNs = 20000;  // longest single hardware sleep of a 
 struct TcParams {
   const __nv_bfloat16* q;
   __nv_bfloat16* out;
-  float* ws;  // lse [splits][rows], then fp16 partials (see internal.h)
+  float* ws;  // lse [splits][rows], then bf16 partials (see internal.h)
   const int32_t* parent;
   int32_t* dev_status;
   int32_t n, hq, hkv, prefix, keys, keys_per_split, splits, rows_per_head;
@@ -137,7 +137,7 @@ struct Layout {
   static constexpr uint32_t kPar = kV + kStages * kKV;
   static constexpr uint32_t kPtab = kPar + kMaxNodes * 4;   // the CTA's page-table slice
   static constexpr uint32_t kBar = kPtab + (PAGED ? kMaxPageSlots * 4 : 0);
-  static constexpr uint32_t kNumBars = 3 * kTiles + 4 * kStages + kTiles + 2;
+  static constexpr uint32_t kNumBars = 3 * kTiles + 4 * kStages + kTiles + 3;
   static constexpr uint32_t kMisc = kBar + kNumBars * 8;
   static constexpr uint32_t kBytes = kMisc + 16;
   static constexpr uint32_t kAlloc = kBytes + 1024;  // slack to align the base to 1024
@@ -159,6 +159,8 @@ struct Bars {
   __device__ uint32_t q_full() const { return base + 8 * (4 * kTiles + 4 * kStages); }
   // a PV product has completed (one tile with double-buffered scores)
   __device__ uint32_t o_done() const { return base + 8 * (4 * kTiles + 4 * kStages + 1); }
+  // after an abort: every MMA the issuing thread has started is complete
+  __device__ uint32_t drain() const { return base + 8 * (4 * kTiles + 4 * kStages + 2); }
 };
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -174,6 +176,18 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
   }
   return true;
+}
+
+// A wait on the teardown path after an abort: for this thread's own copies
+// or MMAs, which complete by themselves; bounded all the same.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int32_t* dev_status) {
+  const long long t0 = clock64();
+  while (!ptx::mbar_try_wait_sleep(bar, parity, kSleepHintNs)) {
+    if (clock64() - t0 > kWaitCycles) {
+      report(dev_status, TV_ERR_TIMEOUT);
+      return;
+    }
+  }
 }
 
 __device__ __forceinline__ uint32_t pick(const uint32_t (&a)[kMaskWords], int i) {
@@ -207,11 +221,6 @@ __device__ __forceinline__ uint32_t visible32(const uint32_t (&anc)[kMaskWords],
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
@@ -275,6 +284,7 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
     }
     ptx::mbar_init(bars.q_full(), 1);
     ptx::mbar_init(bars.o_done(), 1);
+    ptx::mbar_init(bars.drain(), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -314,16 +324,22 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
                          g, page[h]);
   };
   // The producer thread (tid 0) starts streaming K/V at once: the first
-  // kStages blocks need no free slot and do not depend on Q.
+  // kStages blocks need no free slot and do not depend on Q.  It counts what
+  // it has requested, so that after an abort it can wait for its own copies
+  // to land before the CTA exits.
+  int k_last = -1, v_last = -1;  // last K and V block requested
+  bool q_requested = false;
   auto load_k = [&](int j) {
     const int s = j % kStages;
     ptx::mbar_arrive_expect_tx(bars.k_full(s), L::kKV);
     load_block(kmap, base + L::kK + s * L::kKV, bars.k_full(s), j, j == 0);
+    k_last = j;
   };
   auto load_v = [&](int j) {
     const int s = j % kStages;
     ptx::mbar_arrive_expect_tx(bars.v_full(s), L::kKV);
     load_block(vmap, base + L::kV + s * L::kKV, bars.v_full(s), j, false);
+    v_last = j;
   };
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
@@ -339,6 +355,7 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
     // KV head g: one box per 64-column chunk over Q seen as [N][Hq][d], in
     // the 128-byte-swizzled K-major layout; nodes past the tree read as zero.
     ptx::mbar_arrive_expect_tx(bars.q_full(), ntiles * L::kQTile);
+    q_requested = true;
     for (int t = 0; t < ntiles; ++t)
 #pragma unroll
       for (int c = 0; c < D / 64; ++c)
@@ -374,7 +391,8 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
         const int rem = e - t * (kBM * kPieces);
         const int r = rem / kPieces, c = rem - r * kPieces;
         const int grow = row0 + t * kBM + r;
-        if (t < ntiles && grow < p.rows_per_head) {
+        if (t < ntiles && grow < p.rows_per_head &&
+            guard(grow / G < p.n && g * G + (grow % G) < p.hq, p.dev_status)) {
           const int node = grow / G, j = grow - node * G;
           v[i] = __ldg(reinterpret_cast<const uint4*>(
                            p.q + ((size_t)node * p.hq + (size_t)g * G + j) * D) + c);
@@ -688,7 +706,8 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
       // Stage this thread's normalised row as 16-bit values in shared memory
       // (the Q tiles are free: every MMA has completed), then copy the tile
       // out.  With one split the result is the final bf16 output; otherwise
-      // it is the split's fp16 partial plus its log-sum-exp.
+      // it is the split's bf16 partial plus its log-sum-exp (bf16 keeps
+      // float32's exponent range, so any finite V gives a finite partial).
       constexpr int kChunks = D / 8;
       const bool to_out = p.splits == 1;
       const size_t rows_all = (size_t)p.n * p.hq;
@@ -709,7 +728,7 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
             for (int e = 0; e < 4; ++e) {
               const float a = __uint_as_float(v[8 * cc + 2 * e]) * inv;
               const float b = __uint_as_float(v[8 * cc + 2 * e + 1]) * inv;
-              w[e] = to_out ? pack_bf16x2(a, b) : pack_f16x2(a, b);
+              w[e] = pack_bf16x2(a, b);
             }
             const int k = q * 4 + cc;  // 16-byte chunk of the row
             if (p.q_tma) {
@@ -727,7 +746,9 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
           }
         }
         if (p.q_tma) ptx::fence_proxy_async_smem();
-        if (!to_out && row_ok) {
+        if (!to_out && row_ok &&
+            guard(split < p.splits && (size_t)(grow / G) * p.hq + (size_t)g * G + grow % G <
+                                          rows_all, p.dev_status)) {
           const int node = grow / G, jj = grow - node * G;
           const size_t prow = (size_t)node * p.hq + (size_t)g * G + jj;
           p.ws[(size_t)split * rows_all + prow] =
@@ -760,7 +781,8 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
           const int rl = idx / kChunks, ch = idx - rl * kChunks;
           const int Rr = t * kBM + rl;
           const int gr = row0 + Rr;
-          if (gr < p.rows_per_head) {
+          if (gr < p.rows_per_head &&
+              guard((size_t)(gr / G) * p.hq + (size_t)g * G + gr % G < rows_all, p.dev_status)) {
             const int node = gr / G, jj = gr - node * G;
             const size_t prow = (size_t)node * p.hq + (size_t)g * G + jj;
             const uint4 v = *reinterpret_cast<const uint4*>(sm + L::kQ + (size_t)Rr * (D * 2) +
@@ -774,6 +796,28 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
 
   ptx::tc_fence_before();
   __syncthreads();
+  if (*abort_flag) {
+    // A wait ran out and the roles stopped early.  No CTA exits with its own
+    // copies or MMAs in flight: the producer waits for every K, V and Q copy
+    // it requested to land in shared memory, the MMA thread for every MMA it
+    // issued (one commit covers them all), and only then is TMEM freed.
+    if (tid == 0) {
+      for (int s = 0; s < kStages; ++s) {
+        // the last block requested into slot s is the newest phase there
+        const int jk = k_last - ((k_last - s) % kStages + kStages) % kStages;
+        if (k_last >= 0 && jk >= 0) drain_wait(bars.k_full(s), (jk / kStages) & 1, p.dev_status);
+        const int jv = v_last - ((v_last - s) % kStages + kStages) % kStages;
+        if (v_last >= 0 && jv >= 0) drain_wait(bars.v_full(s), (jv / kStages) & 1, p.dev_status);
+      }
+      if (q_requested) drain_wait(bars.q_full(), 0, p.dev_status);
+    }
+    if (warp == 1 && lane == 0) {
+      ptx::mma_commit(bars.drain());
+      drain_wait(bars.drain(), 0, p.dev_status);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
@@ -816,11 +860,10 @@ bool make_paged_kv_map(CUtensorMap* map, const void* base, int d, int page_size,
 // 3-D map over Q [n][hq][d] (bf16): boxes of 64 columns x G heads x 128/G
 // nodes (one 128-row tile of a KV head's query group), 128-byte swizzle,
 // nodes past the tree read as zero.
-// 4-D map over an output-shaped array [layers][n][hq][d] of 16-bit values
-// (the fp16 split partials, or the bf16 output with one layer): boxes of 64
-// columns x G heads x 128/G nodes x 1, no swizzle change from the Q tiles.
-bool make_o_map(CUtensorMap* map, void* base, bool fp16, int d, int n, int hq, int group,
-                int layers) {
+// 4-D map over an output-shaped array [layers][n][hq][d] of bf16 values
+// (the split partials, or the output with one layer): boxes of 64 columns x
+// G heads x 128/G nodes x 1, no swizzle change from the Q tiles.
+bool make_o_map(CUtensorMap* map, void* base, int d, int n, int hq, int group, int layers) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)hq, (cuuint64_t)n, (cuuint64_t)layers};
@@ -828,7 +871,7 @@ bool make_o_map(CUtensorMap* map, void* base, bool fp16, int d, int n, int hq, i
                                  (cuuint64_t)n * hq * d * 2};
   const cuuint32_t box[4] = {64, (cuuint32_t)group, (cuuint32_t)(kBM / group), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(map, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base,
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base,
             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -903,7 +946,7 @@ bool fill_request(const AttnProblem& p, const SplitPlan& plan, float* ws, CUtens
     void* obase = to_out ? p.out
                          : static_cast<void*>(reinterpret_cast<uint8_t*>(ws) +
                                               partial_o_offset(plan.splits, (size_t)p.n * p.hq));
-    if (!make_o_map(omap, obase, !to_out, D, p.n, p.hq, group, to_out ? 1 : plan.splits))
+    if (!make_o_map(omap, obase, D, p.n, p.hq, group, to_out ? 1 : plan.splits))
       return false;
   } else {
     memset(omap, 0, sizeof(*omap));

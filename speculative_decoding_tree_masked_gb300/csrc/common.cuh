@@ -17,6 +17,18 @@ __device__ __forceinline__ void report(int32_t* dev_status, int32_t code) {
   if (dev_status != nullptr) atomicCAS(dev_status, 0, code);
 }
 
+// Checked build (-DTV_CHECKED=1): guard(ok, st) records TV_ERR_BOUNDS when
+// an index test fails and returns false, so that the caller skips the
+// access.  In a normal build it is the constant true and the test vanishes.
+#ifndef TV_CHECKED
+#define TV_CHECKED 0
+#endif
+__device__ __forceinline__ bool guard(bool ok, int32_t* dev_status) {
+  if (!TV_CHECKED) return true;
+  if (!ok) report(dev_status, TV_ERR_BOUNDS);
+  return ok;
+}
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ void store_f32(float* p, float v) { *p = v; }

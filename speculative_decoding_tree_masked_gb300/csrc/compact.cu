@@ -94,13 +94,20 @@ compact_kernel(const __grid_constant__ CompactJobs<MAXB> jobs, int hkv, int row_
   __syncthreads();
   const int moves = count;
   const int chunks = row_bytes >> 4;
+  // checked build: a moving row stays inside the tree's rows [P, P + n) of
+  // its head (contiguous caches), and the staging buffer holds n rows
+  auto row_ok = [&](int r) {
+    return guard(r >= prefix && r < prefix + n && r < job.cap && moves <= n, dev_status);
+  };
   for (int e = tid; e < moves * chunks; e += kCompactThreads) {
     const int r = e / chunks, c = e - r * chunks;
+    if (page_table == nullptr && !row_ok(src_row[r])) continue;
     buf[e] = reinterpret_cast<const uint4*>(lbase + row_at(src_row[r]))[c];
   }
   __syncthreads();
   for (int e = tid; e < moves * chunks; e += kCompactThreads) {
     const int r = e / chunks, c = e - r * chunks;
+    if (page_table == nullptr && !row_ok(dst_row[r])) continue;
     reinterpret_cast<uint4*>(lbase + row_at(dst_row[r]))[c] = buf[e];
   }
 }

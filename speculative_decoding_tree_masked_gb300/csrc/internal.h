@@ -64,8 +64,9 @@ SplitPlan plan_attention(int32_t n, int32_t hq, int32_t hkv, int32_t d, int32_t 
 //                    log2-scaled score units (-inf when the split holds no
 //                    key the row may see)
 //   o   [splits][R][d]  the split's normalised output: fp32 for fp32
-//                    attention, fp16 for bf16 attention; starts at byte
-//                    partial_o_offset(splits, R)
+//                    attention, bf16 for bf16 attention (float32's exponent
+//                    range, so a finite V never overflows a partial); starts
+//                    at byte partial_o_offset(splits, R)
 __host__ __device__ inline size_t partial_o_offset(int splits, size_t rows) {
   return ((size_t)splits * rows * sizeof(float) + 255) & ~size_t(255);
 }
