@@ -94,6 +94,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr uint32_t kSleepHintNs = 20000;  // longest single hardware sleep of a wait
+// A/B switch: where dependents are signalled (0 after the last product, 1 after the output store)
+constexpr int kTriggerAt = 0;
 
 struct TcParams {
   const __nv_bfloat16* q;
@@ -300,28 +302,28 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
   int32_t* ptab = reinterpret_cast<int32_t*>(sm + L::kPtab);
   auto load_block = [&](const CUtensorMap* map, uint32_t dst, uint32_t bar, int j,
                         bool table_in_global) {
-    if (!paged) {
+    if constexpr (!paged) {
 #pragma unroll
       for (int c = 0; c < D / 64; ++c)
         ptx::tma_load_3d(dst + c * (kBN * 128), map, bar, c * 64, kbeg + j * kBN, g);
-      return;
+    } else {
+      // both pages are looked up before either copy is issued, so that the
+      // table reads overlap
+      int page[kHalves], off[kHalves];
+#pragma unroll
+      for (int h = 0; h < kHalves; ++h) {
+        const int row = min(kbeg + j * kBN + h * kPageRows, last64);
+        const int slot = row / p.page_size;
+        page[h] = table_in_global ? __ldg(p.page_table + slot) : ptab[slot - pfirst];
+        off[h] = row - slot * p.page_size;
+      }
+#pragma unroll
+      for (int h = 0; h < kHalves; ++h)
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          ptx::tma_load_4d(dst + c * (kBN * 128) + h * (kPageRows * 128), map, bar, c * 64,
+                           off[h], g, page[h]);
     }
-    // both pages are looked up before either copy is issued, so that the
-    // table reads overlap
-    int page[kHalves], off[kHalves];
-#pragma unroll
-    for (int h = 0; h < kHalves; ++h) {
-      const int row = min(kbeg + j * kBN + h * kPageRows, last64);
-      const int slot = row / p.page_size;
-      page[h] = table_in_global ? __ldg(p.page_table + slot) : ptab[slot - pfirst];
-      off[h] = row - slot * p.page_size;
-    }
-#pragma unroll
-    for (int h = 0; h < kHalves; ++h)
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        ptx::tma_load_4d(dst + c * (kBN * 128) + h * (kPageRows * 128), map, bar, c * 64, off[h],
-                         g, page[h]);
   };
   // The producer thread (tid 0) starts streaming K/V at once: the first
   // kStages blocks need no free slot and do not depend on Q.  It counts what
@@ -344,6 +346,26 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
     ptx::tmem_relinquish();
+  }
+  if constexpr (!PAGED) {
+    // While an earlier kernel on the stream may still run, warm L2 with the
+    // boxes this CTA loads first (its Q tiles, K and V of its first block,
+    // K of its second).  A prefetch returns nothing to the CTA and L2 is
+    // where every write lands, so it cannot make a later load see stale
+    // data; it only moves the first loads' DRAM latency off the critical
+    // path.  (Warming more blocks ahead, or the whole key range, measured
+    // slower: the extra requests delay the first loads.)
+    if (tid == 0 && nb > 0) {
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        ptx::tma_prefetch_l2_3d(kmap, c * 64, kbeg, g);
+        ptx::tma_prefetch_l2_3d(vmap, c * 64, kbeg, g);
+        if (nb > 1) ptx::tma_prefetch_l2_3d(kmap, c * 64, kbeg + kBN, g);
+        if (p.q_tma)
+          for (int t = 0; t < ntiles; ++t)
+            ptx::tma_prefetch_l2_3d(qmap, c * 64, g * G, (row0 + t * kBM) / G);
+      }
+    }
   }
   // Everything above reads nothing an earlier kernel may write.  The kernel
   // is launched under programmatic stream serialization, so it may start
@@ -703,6 +725,12 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
       }
       // epilogue: O_t is final once the last PV has completed
       if (ok) ok = wait_bar(bars.o_final(t), 0, abort_flag, p.dev_status);
+      // Every product of the CTA is done once the last tile's O is final: a
+      // kernel launched after this one under programmatic serialization (the
+      // combine of the splits) may be scheduled now; it waits for this grid
+      // to complete before it reads anything.  One thread signals.
+      if (kTriggerAt == 0 && t == ntiles - 1 && (sw & 3) == 0 && lane == 0)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
       // Stage this thread's normalised row as 16-bit values in shared memory
       // (the Q tiles are free: every MMA has completed), then copy the tile
       // out.  With one split the result is the final bf16 output; otherwise
@@ -716,18 +744,23 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
         ptx::tc_fence_after();
         const float inv = l > 0.f ? 1.f / l : 0.f;
         uint8_t* srow = sm + L::kQ + (size_t)R * (D * 2);
+        // the whole row in one TMEM load and one wait
+        uint32_t v[D];
+        if constexpr (D == 128) {
+          ptx::tmem_ld128(t_o, v);
+        } else {
+          ptx::tmem_ld64(t_o, v);
+        }
+        ptx::tmem_wait_ld(v);
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
-          uint32_t v[32];
-          ptx::tmem_ld32(t_o + q * 32, v);
-          ptx::tmem_wait_ld(v);
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float a = __uint_as_float(v[8 * cc + 2 * e]) * inv;
-              const float b = __uint_as_float(v[8 * cc + 2 * e + 1]) * inv;
+              const float a = __uint_as_float(v[32 * q + 8 * cc + 2 * e]) * inv;
+              const float b = __uint_as_float(v[32 * q + 8 * cc + 2 * e + 1]) * inv;
               w[e] = pack_bf16x2(a, b);
             }
             const int k = q * 4 + cc;  // 16-byte chunk of the row
@@ -794,6 +827,7 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
     }
   }
 
+  if (kTriggerAt == 1 && tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   ptx::tc_fence_before();
   __syncthreads();
   if (*abort_flag) {
