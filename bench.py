@@ -49,17 +49,23 @@ def _visible_pairs(parent, prefix, hq):
 
 
 MUFU_EX2_PER_CLK_SM = 16  # ex2 results per clock per SM (special-function units)
-SMS = 152
 
 
-def _bounds_us(nbytes, flops, exps, peaks):
+def _sm_count():
+    """SMs of the current GPU (read at run time)."""
+    import torch
+    return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+
+
+def _bounds_us(nbytes, flops, exps, peaks, sms=None):
     """Lower bounds on one attention call's time (us): HBM bytes at the
     measured copy bandwidth, flops at the measured bf16 rate, and one ex2 per
-    visible (row, key) pair on the special-function units at the maximum
-    SM clock."""
+    visible (row, key) pair on the special-function units of every SM (the
+    current GPU's count unless `sms` is given) at the maximum SM clock."""
+    sms = _sm_count() if sms is None else sms
     return {"hbm": nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6,
             "tensor": flops / (peaks["bf16_tflops"] * 1e12) * 1e6,
-            "exp": exps / (MUFU_EX2_PER_CLK_SM * SMS * peaks["sm_max_mhz"] * 1e6) * 1e6}
+            "exp": exps / (MUFU_EX2_PER_CLK_SM * sms * peaks["sm_max_mhz"] * 1e6) * 1e6}
 
 
 def _peaks():
@@ -279,13 +285,64 @@ def torch_int16():
     return torch.int16
 
 
-def _oracle_subprocess(nodes, layers, repeats, workers=0):
-    """oracle_sample (workers 0) or oracle_sample_all_cores in a fresh CPU-only
-    process with one BLAS thread per process."""
+# The other single-GPU workloads, timed beside the full step (GPU and oracle).
+CONFIGS = {
+    "tiny": "tiny: 4/1 heads, d64, fp32, prefix 128, 15-node complete binary tree, vocab 1000; "
+            "attention, greedy acceptance, compaction",
+    "l3_8b": "Llama-3-8B-shaped verify: 32/8 heads, d128, bf16, prefix 2048, 64-node tree "
+             "(depth <= 8, fan-out <= 8), 1 layer, vocab 128256; attention, greedy acceptance, "
+             "compaction",
+    "l3_70b": "Llama-3-70B-shaped verify: 64/8 heads, d128, bf16, prefix 8192, 64-node tree "
+              "(8 expansions of width 8), 8 layers of KV; attention of every layer",
+}
+
+
+def oracle_config_sample(name: str, seed: int = 0) -> dict:
+    """The oracle on a bounded sample of one step of a named workload, scaled
+    to the whole step: attention of a subset of the tree's nodes in one
+    layer (all nodes for tiny), then acceptance and compaction in full when
+    the workload has logits."""
+    import numpy as np
+    import oracle
+    from workloads import synth
+    w = synth.make_workload(name, seed=seed)
+    nodes = {"tiny": w.n, "l3_8b": 16, "l3_70b": 4}[name]
+    sample_nodes = list(range(0, w.n, max(1, w.n // nodes)))[:nodes]
+    q, k, v = synth.make_qkv(w, layer=0)
+    qn, kn, vn = q.float().numpy(), k.float().numpy(), v.float().numpy()
+    reps, t_attn = 0, 0.0
+    while t_attn < 0.5 or reps < 1:
+        t0 = time.perf_counter()
+        oracle.tree_attention(qn, kn, vn, w.prefix, w.parent, nodes=sample_nodes)
+        t_attn += time.perf_counter() - t0
+        reps += 1
+    t_attn /= reps
+    t_rest = 0.0
+    if w.logits is not None:
+        t0 = time.perf_counter()
+        res = oracle.tree_accept(w.logits, w.token, w.parent, w.prefix)
+        view = np.int32 if w.dtype == "f32" else np.int16
+        for cache in (kn.view(view) if w.dtype == "f32" else k.view(torch_int16()).numpy(),
+                      vn.view(view) if w.dtype == "f32" else v.view(torch_int16()).numpy()):
+            oracle.kv_compact(cache, w.prefix, res["new_pos"])
+        t_rest = time.perf_counter() - t0
+    t_step = t_attn * (w.n / len(sample_nodes)) * w.layers + t_rest
+    what = "attention of %d of %d tree nodes x 1 of %d layers%s; scaled to one step" % (
+        len(sample_nodes), w.n, w.layers,
+        ", full acceptance and compaction" if w.logits is not None else "")
+    return {"tree_tokens_per_s": w.n / t_step, "s_per_step": t_step, "cores": 1,
+            "kind": "oracle", "sample": what}
+
+
+def _oracle_subprocess(nodes, layers, repeats, workers=0, call=None):
+    """oracle_sample (workers 0) or oracle_sample_all_cores (or the given call
+    of this module, with r the repeat index) in a fresh CPU-only process with
+    one BLAS thread per process."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    call = ("bench.oracle_sample(%d, %d, seed=r)" % (nodes, layers) if workers == 0 else
-            "bench.oracle_sample_all_cores(%d, %d, %d, seed=r)" % (nodes, layers, workers))
+    if call is None:
+        call = ("bench.oracle_sample(%d, %d, seed=r)" % (nodes, layers) if workers == 0 else
+                "bench.oracle_sample_all_cores(%d, %d, %d, seed=r)" % (nodes, layers, workers))
     code = ("import json, sys; sys.path.insert(0, %r); import bench\n"
             "if __name__ == '__main__':\n"
             "    print(json.dumps([%s for r in range(%d)]))" % (ROOT, call, repeats))
@@ -529,6 +586,9 @@ def run_gpu(args, rank, world, local_rank):
     e2e = None
     if not args.no_e2e:
         e2e = _end_to_end(args, world, dev, stream, step, q, logits, token, parent, acc, w)
+    configs = None
+    if not args.no_configs and rank == 0:
+        configs = run_configs(args, dev, stream, _peaks())
 
     torch.cuda.synchronize()
     if int(status.item()) != 0:
@@ -548,8 +608,8 @@ def run_gpu(args, rank, world, local_rank):
         roof = {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s"}
     else:
-        # fp32 FMA pipes: 152 SMs x 128 lanes x 2 flops x max SM clock
-        alu_peak = 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+        # fp32 FMA pipes: SMs x 128 lanes x 2 flops x max SM clock
+        alu_peak = _sm_count() * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
         roof = {"bound": "alu", "achieved": tflops, "peak": alu_peak, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = _profiled_traffic()
@@ -599,12 +659,155 @@ def run_gpu(args, rank, world, local_rank):
                       "hbm_frac": gbs / peaks["hbm_gbs"], "tflops": tflops,
                       "tensor_frac": tflops / peaks["bf16_tflops"],
                       "bounds_us": bounds, "binding_frac": max(bounds.values()) /
-                      (attn_ms_layer * 1e3)},
+                      (attn_ms_layer * 1e3),
+                      "hbm_ceiling": bounds["hbm"] / max(bounds.values())},
+        "configs": configs,
     })
     print(json.dumps(line), flush=True)
 
 
-SWEEP_PREFIXES = (1024, 4096, 16384, 32768)
+L2_BYTES = 130_000_000
+
+
+def _timed_us(graph, stream, iters, flush=None):
+    """Median device time (us) of one replay of `graph` (events on `stream`);
+    with `flush`, a read of that buffer (larger than L2, so it leaves L2
+    holding clean lines of its own) precedes every timed replay."""
+    import statistics
+
+    import torch
+    times = []
+    with torch.cuda.stream(stream):
+        for _ in range(iters):
+            if flush is not None:
+                flush.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            times.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) * 1e3 for a, b in times)
+
+
+def run_configs(args, dev, stream, peaks):
+    """GPU timing of the tiny, Llama-3-8B- and Llama-3-70B-shaped workloads,
+    with the oracle timed on a bounded sample of each on one host core.
+
+    Each workload's step (and its attention alone) is captured as a CUDA
+    graph over several copies of its inputs, one step per copy, so that one
+    replay reads more than L2 holds; a workload whose copies cannot exceed
+    L2 cheaply (tiny) runs on one copy with L2 flushed by a large read before
+    every timed replay."""
+    import math
+
+    import torch
+
+    import speculative_decoding_tree_masked_gb300 as tvp
+    from workloads import synth
+
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out_all = {}
+    for name, what in CONFIGS.items():
+        w = synth.make_workload(name, seed=args.seed)
+        q0, k0, v0 = synth.make_qkv(w)
+        elem = 4 if w.dtype == "f32" else 2
+        step_bytes = (q0.numel() + k0.numel() + v0.numel()) * elem + \
+            (w.logits.nbytes if w.logits is not None else 0)
+        copies = max(2, math.ceil(2.5 * L2_BYTES / step_bytes))
+        flush = None
+        if copies > 16:
+            copies = 1
+            flush = torch.ones(512 << 20, dtype=torch.float16, device=dev)
+        has_accept = w.logits is not None
+        sets = []
+        for _ in range(copies):
+            c = {"q": q0.to(dev), "k": k0.to(dev), "v": v0.to(dev),
+                 "parent": torch.from_numpy(w.parent).to(dev)}
+            c["out"] = torch.empty_like(c["q"])
+            if has_accept:
+                c["logits"] = torch.from_numpy(w.logits).to(dev)
+                c["token"] = torch.from_numpy(w.token).to(dev)
+            sets.append(c)
+        ws = tvp.attn_workspace(w.n, w.hq, w.hkv, w.d, sets[0]["q"].dtype, w.prefix, dev)
+
+        def attention():
+            for c in sets:
+                for layer in range(w.layers):
+                    tvp.tree_attn_verify(c["q"][layer], c["k"][layer], c["v"][layer], w.prefix,
+                                         c["parent"], out=c["out"][layer], workspace=ws,
+                                         status=status)
+
+        def step():
+            for c in sets:
+                for layer in range(w.layers):
+                    tvp.tree_attn_verify(c["q"][layer], c["k"][layer], c["v"][layer], w.prefix,
+                                         c["parent"], out=c["out"][layer], workspace=ws,
+                                         status=status)
+                if has_accept:
+                    acc = tvp.tree_accept(c["logits"], c["token"], c["parent"], w.prefix,
+                                          status=status)
+                    tvp.kv_compact(c["k"], c["v"], w.prefix, w.n, acc["new_pos"],
+                                   status=status)
+
+        graphs = {}
+        with torch.cuda.stream(stream):
+            step()
+        torch.cuda.synchronize()
+        for key, fn in (("step", step), ("attention", attention)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            graphs[key] = g
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                graphs["step"].replay()
+        torch.cuda.synchronize()
+        iters = 30 if flush is None else 100
+        step_us = _timed_us(graphs["step"], stream, iters, flush) / copies
+        attn_us = _timed_us(graphs["attention"], stream, iters, flush) / (copies * w.layers)
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {int(status.item())} in workload {name}")
+        nbytes, flops = _algorithmic_work(w.parent, w.prefix, w.n, w.hq, w.hkv, w.d, elem)
+        bounds = _bounds_us(nbytes, flops, _visible_pairs(w.parent, w.prefix, w.hq), peaks)
+        if w.dtype == "f32":
+            bounds.pop("tensor")  # fp32 runs on the FMA pipes
+            alu_peak = _sm_count() * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+            bounds["alu"] = flops / (alu_peak * 1e12) * 1e6
+        binding = max(bounds, key=bounds.get)
+        res = {"workload": what, "us_per_step": step_us,
+               "tree_tokens_per_s": w.n / (step_us * 1e-6),
+               "verify_steps_per_s": 1e6 / step_us,
+               "attention": {"us_per_layer": attn_us,
+                             "hbm_gbs": nbytes / attn_us / 1e3,
+                             "hbm_frac": nbytes / attn_us / 1e3 / peaks["hbm_gbs"],
+                             "tflops": flops / attn_us / 1e6,
+                             "bounds_us": bounds, "bound": binding,
+                             "binding_frac": bounds[binding] / attn_us,
+                             "hbm_ceiling": bounds["hbm"] / bounds[binding],
+                             "splits": tvp.attn_plan(w.n, w.hq, w.hkv, w.d, sets[0]["q"].dtype,
+                                                     w.prefix)["splits"]},
+               "timing": (f"CUDA graph over {copies} copies of the inputs "
+                          f"({copies * step_bytes / 1e6:.0f} MB, more than L2), "
+                          f"median of {iters} replays" if flush is None else
+                          f"CUDA graph, L2 flushed by a 1 GB read before each of {iters} "
+                          "timed replays, median")}
+        if w.dtype != "f32":
+            res["attention"]["tensor_frac"] = flops / attn_us / 1e6 / peaks["bf16_tflops"]
+        out_all[name] = res
+        del sets, ws, graphs, flush
+        torch.cuda.empty_cache()
+    if not args.no_cpu_baseline:
+        for name in CONFIGS:
+            try:
+                o = _oracle_subprocess(0, 0, 1, call=f"bench.oracle_config_sample({name!r})")[0]
+                out_all[name]["oracle"] = o
+            except Exception as e:
+                out_all[name]["oracle"] = {"error": str(e)[-300:]}
+    return out_all
+
+
+SWEEP_PREFIXES = (1024, 4096, 8192, 16384, 32768)
 SWEEP_NODES = (8, 32, 64, 128)
 
 
@@ -716,9 +919,11 @@ def run_sweep(args, local_rank):
             if int(status.item()) != 0:
                 raise RuntimeError(f"device status {int(status.item())} in the sweep")
             us = ea.elapsed_time(eb) * 1e3 / (reps * copies)
-            sdpa_us = _sdpa_us(q, ks, vs, prefix, w.parent, copies, reps, args.warmup, stream)
-            flash_us = _sdpa_us(q, ks, vs, prefix, w.parent, copies, reps, args.warmup, stream,
-                                masked=False)
+            sdpa_us = flash_us = None
+            if args.sdpa:
+                sdpa_us = _sdpa_us(q, ks, vs, prefix, w.parent, copies, reps, args.warmup, stream)
+                flash_us = _sdpa_us(q, ks, vs, prefix, w.parent, copies, reps, args.warmup,
+                                    stream, masked=False)
             nbytes, flops = _algorithmic_work(w.parent, prefix, n, w.hq, w.hkv, w.d)
             bounds = _bounds_us(nbytes, flops, _visible_pairs(w.parent, prefix, w.hq), peaks)
             binding = max(bounds, key=bounds.get)
@@ -1149,7 +1354,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -1169,6 +1374,11 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="time the attention alone over the prefix x tree-size sweep "
                          "(one JSON line per configuration) instead of the step")
+    ap.add_argument("--sdpa", action="store_true",
+                    help="with --sweep: also time PyTorch's SDPA on the same inputs (context)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="leave out the other workloads' timings (tiny, Llama-3-8B- and "
+                         "Llama-3-70B-shaped) from the default line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

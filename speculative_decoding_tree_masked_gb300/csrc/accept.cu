@@ -23,6 +23,7 @@ namespace {
 
 constexpr int kArgmaxCluster = 8;
 constexpr int kArgmaxThreads = 256;
+constexpr int kArgmaxLoads = 8;  // float4 loads in flight per thread
 
 // True if (a, ia) comes before (b, ib) in NumPy argmax order: a NaN beats any
 // number, larger values beat smaller ones, and ties go to the lower index.
@@ -41,6 +42,11 @@ argmax_kernel(const float* __restrict__ logits, int vocab, int32_t* __restrict__
   __shared__ int s_idx[kArgmaxThreads / 32];
   __shared__ float c_val;
   __shared__ int c_idx;
+  // launched under programmatic serialization: the walk that follows may be
+  // scheduled now (it waits for this grid); this grid waits for the kernel
+  // before it (which may write the logits) before reading anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int row = blockIdx.y;
@@ -60,10 +66,11 @@ argmax_kernel(const float* __restrict__ logits, int vocab, int32_t* __restrict__
     // which takes the element-wise order
     const float4* b4 = reinterpret_cast<const float4*>(base);
     const int e4 = end / 4;
-    for (int i40 = beg / 4 + tid; i40 < e4; i40 += 8 * kArgmaxThreads) {
-      float z[32];
+    constexpr int kZ = 4 * kArgmaxLoads;
+    for (int i40 = beg / 4 + tid; i40 < e4; i40 += kArgmaxLoads * kArgmaxThreads) {
+      float z[kZ];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
+      for (int q = 0; q < kArgmaxLoads; ++q) {
         const int i4 = i40 + q * kArgmaxThreads;
         const float4 x = i4 < e4 ? __ldcs(b4 + i4)
                                  : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
@@ -76,23 +83,23 @@ argmax_kernel(const float* __restrict__ logits, int vocab, int32_t* __restrict__
       bool nan = false;
       float bm = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
+      for (int k = 0; k < kZ; ++k) {
         nan |= isnan(z[k]);
         bm = fmaxf(bm, z[k]);
       }
       if (nan) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
+        for (int k = 0; k < kZ; ++k)
           if (i40 + (k >> 2) * kArgmaxThreads < e4 && better(z[k], index_of(k), bv, bi)) {
             bv = z[k];
             bi = index_of(k);
           }
       } else {
-        int first = 32;
+        int first = kZ;
 #pragma unroll
-        for (int k = 31; k >= 0; --k)
+        for (int k = kZ - 1; k >= 0; --k)
           if (z[k] == bm) first = k;
-        if (first < 32 && i40 + (first >> 2) * kArgmaxThreads < e4 &&
+        if (first < kZ && i40 + (first >> 2) * kArgmaxThreads < e4 &&
             better(bm, index_of(first), bv, bi)) {
           bv = bm;
           bi = index_of(first);
@@ -146,6 +153,11 @@ walk_kernel(const __grid_constant__ WalkJobs jobs, const int32_t* __restrict__ t
             int32_t* new_parent, int32_t* n_surv, int32_t* dev_status) {
   __shared__ int32_t par[kMaxNodes], tok[kMaxNodes], amv[kMaxNodes], rank_of[kMaxNodes];
   __shared__ int32_t plist[kMaxNodes];
+  // launched under programmatic serialization after the argmax (or the
+  // sampling): wait for it; a compaction launched after this kernel may be
+  // scheduled now and waits for it in turn
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x;
   const int b = blockIdx.x;
   const int o = jobs.off[b];
@@ -283,9 +295,8 @@ cudaError_t launch_accept_batched(const float* logits, int32_t vocab, const int3
                                   int32_t* am, int32_t* m, int32_t* path, int32_t* out_tokens,
                                   int32_t* new_pos, int32_t* new_parent, int32_t* n_survivors,
                                   int32_t* dev_status, cudaStream_t s) {
-  argmax_kernel<<<dim3(kArgmaxCluster, node_offset[batch]), kArgmaxThreads, 0, s>>>(
-      logits, vocab, am);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(argmax_kernel, dim3(kArgmaxCluster, node_offset[batch]),
+                             dim3(kArgmaxThreads), 0, s, logits, vocab, am);
   if (e != cudaSuccess) return e;
   return launch_walk_batched(token, parent, am, batch, node_offset, vocab, prefix, m, path,
                              out_tokens, new_pos, new_parent, n_survivors, dev_status, s);
@@ -311,9 +322,8 @@ cudaError_t launch_walk_batched(const int32_t* token, const int32_t* parent, con
     jobs.prefix[b] = prefix[b];
   }
   jobs.off[batch] = node_offset[batch];
-  walk_kernel<<<batch, 32, 0, s>>>(jobs, token, parent, am, vocab, m, path, out_tokens, new_pos,
-                                   new_parent, n_survivors, dev_status);
-  return cudaGetLastError();
+  return launch_pdl(walk_kernel, dim3(batch), dim3(32), 0, s, jobs, token, parent, am, vocab, m,
+                    path, out_tokens, new_pos, new_parent, n_survivors, dev_status);
 }
 
 }  // namespace tv

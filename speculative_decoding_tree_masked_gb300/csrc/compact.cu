@@ -46,6 +46,9 @@ compact_kernel(const __grid_constant__ CompactJobs<MAXB> jobs, int hkv, int row_
   __shared__ int src_row[kMaxNodes], dst_row[kMaxNodes];
   __shared__ uint32_t used[kMaskWords];
   __shared__ int count;
+  // launched under programmatic serialization after the walk that writes
+  // new_pos: wait for it (and for every earlier kernel) before any access
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const CompactJob& job = jobs.job[blockIdx.y];
   const int prefix = job.prefix, n = job.n;
   const int32_t* __restrict__ new_pos = job.new_pos;
@@ -147,9 +150,8 @@ cudaError_t launch_jobs(const CompactJobs<MAXB>& jobs, int batch, int32_t layers
   }
   const size_t smem = (size_t)max_n * row_bytes;
   const dim3 grid((unsigned)layers * (unsigned)hkv * 2u, (unsigned)batch);
-  compact_kernel<MAXB><<<grid, kCompactThreads, smem, s>>>(jobs, hkv, row_bytes, page_size,
-                                                           num_pages, dev_status);
-  return cudaGetLastError();
+  return launch_pdl(compact_kernel<MAXB>, grid, dim3(kCompactThreads), smem, s, jobs, hkv,
+                    row_bytes, page_size, num_pages, dev_status);
 }
 
 }  // namespace

@@ -229,6 +229,11 @@ expand_chunk_kernel(const float* __restrict__ logits, int vocab, int chunk_len, 
   __shared__ float s_red[kChunkWarps];
   __shared__ float s_out_v[TV_MAX_EXPAND_WIDTH];
   __shared__ int s_out_k[TV_MAX_EXPAND_WIDTH];
+  // launched under programmatic serialization: the merge may be scheduled
+  // now (it waits for this grid); this grid waits for the kernel before it
+  // (which may write the logits) before reading anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int f = blockIdx.y, c = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int beg = c * chunk_len;
   const int len = min(chunk_len, vocab - beg);
@@ -325,6 +330,8 @@ expand_merge_kernel(const float* __restrict__ ws, int nf, int chunks, int w,
   __shared__ float o_s[TV_MAX_EXPAND_WIDTH];
   __shared__ int o_k[TV_MAX_EXPAND_WIDTH];
   __shared__ int s_bad;
+  // launched under programmatic serialization after the slice kernel
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const size_t rw = record_words(w);
   // o / w as a multiply-high by ceil(2^32 / w): exact for o < 2^16 and
@@ -436,6 +443,9 @@ draft_reroot_kernel(const int32_t* __restrict__ parent, const int32_t* __restric
                     int prefix, int32_t* new_pos, int32_t* new_parent, int32_t* new_token,
                     float* new_cum, int32_t* n_surv, int32_t* dev_status) {
   __shared__ int32_t par[kMaxNodes], tok[kMaxNodes], rank_of[kMaxNodes];
+  // launched under programmatic serialization after the walk whose path,
+  // m and out_tokens it reads
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x;
   const int m = *m_in;
   bool ok = m >= 0 && m < n;
@@ -569,13 +579,12 @@ cudaError_t launch_expand(const float* logits, int32_t vocab, int32_t n_frontier
                           int32_t* dev_status, cudaStream_t s) {
   const ExpandPlan pl = plan_expand(n_frontier, vocab, w);
   const dim3 grid(pl.chunks, n_frontier);
-  if (pl.chunk_len <= kShortSlice)
-    expand_chunk_kernel<8><<<grid, kChunkThreads, 0, s>>>(logits, vocab, pl.chunk_len, w,
-                                                           static_cast<float*>(ws));
-  else
-    expand_chunk_kernel<32><<<grid, kChunkThreads, 0, s>>>(logits, vocab, pl.chunk_len, w,
-                                                            static_cast<float*>(ws));
-  cudaError_t e = cudaGetLastError();
+  float* wsf = static_cast<float*>(ws);
+  cudaError_t e = pl.chunk_len <= kShortSlice
+                      ? launch_pdl(expand_chunk_kernel<8>, grid, dim3(kChunkThreads), 0, s,
+                                   logits, vocab, pl.chunk_len, w, wsf)
+                      : launch_pdl(expand_chunk_kernel<32>, grid, dim3(kChunkThreads), 0, s,
+                                   logits, vocab, pl.chunk_len, w, wsf);
   if (e != cudaSuccess) return e;
   static std::atomic<bool> attr_set[64];  // per device (host threads may race here)
   int dev = 0;
@@ -587,10 +596,9 @@ cudaError_t launch_expand(const float* logits, int32_t vocab, int32_t n_frontier
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  expand_merge_kernel<<<1, kMergeThreads, kMergeSmem, s>>>(static_cast<const float*>(ws), n_frontier,
-                                                  pl.chunks, w, frontier, cum, n_nodes,
-                                                  new_parent, new_token, new_score, dev_status);
-  return cudaGetLastError();
+  return launch_pdl(expand_merge_kernel, dim3(1), dim3(kMergeThreads), kMergeSmem, s,
+                    static_cast<const float*>(ws), n_frontier, pl.chunks, w, frontier, cum,
+                    n_nodes, new_parent, new_token, new_score, dev_status);
 }
 
 cudaError_t launch_draft_reroot(const int32_t* parent, const int32_t* token, const float* cum,
@@ -598,10 +606,9 @@ cudaError_t launch_draft_reroot(const int32_t* parent, const int32_t* token, con
                                 const int32_t* out_tokens, int32_t prefix, int32_t* new_pos,
                                 int32_t* new_parent, int32_t* new_token, float* new_cum,
                                 int32_t* n_survivors, int32_t* dev_status, cudaStream_t s) {
-  draft_reroot_kernel<<<1, 32, 0, s>>>(parent, token, cum, n, path, m, out_tokens, prefix,
-                                       new_pos, new_parent, new_token, new_cum, n_survivors,
-                                       dev_status);
-  return cudaGetLastError();
+  return launch_pdl(draft_reroot_kernel, dim3(1), dim3(32), 0, s, parent, token, cum, n, path, m,
+                    out_tokens, prefix, new_pos, new_parent, new_token, new_cum, n_survivors,
+                    dev_status);
 }
 
 }  // namespace tv

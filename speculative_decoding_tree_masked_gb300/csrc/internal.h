@@ -13,6 +13,27 @@
 
 namespace tv {
 
+// Launches `kernel` with programmatic stream serialization: its CTAs may be
+// scheduled once the previous kernel on the stream signals
+// griddepcontrol.launch_dependents (or finishes), so the kernel must execute
+// griddepcontrol.wait before it reads or writes any memory that kernel
+// touches.  The launch gap of a short kernel then overlaps its predecessor.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // The driver's tensor-map encoder (null when the driver does not offer it).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
 

@@ -98,6 +98,10 @@ sample_kernel(const float* __restrict__ logits, int vocab, const __grid_constant
   __shared__ double cta_s;                 // its mass at the row maximum
   __shared__ float cta_m_row;              // the row maximum
   __shared__ int sel_owner, sel_warp;      // the drawing CTA and warp (-1: none)
+  // launched under programmatic serialization: the walk may be scheduled
+  // now; this grid waits for the kernel before it before reading anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ double sel_rem;               // the target mass left inside that warp's run
   cg::cluster_group cluster = cg::this_cluster();
   const int row = blockIdx.y;
@@ -322,9 +326,8 @@ cudaError_t launch_accept_sampled_batched(const float* logits, int32_t vocab,
     jobs.offset[b] = offset[b];
   }
   jobs.off[batch] = node_offset[batch];
-  sample_kernel<<<dim3(kSampleCluster, node_offset[batch]), kSampleThreads, 0, s>>>(
-      logits, vocab, jobs, sampled);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(sample_kernel, dim3(kSampleCluster, node_offset[batch]),
+                             dim3(kSampleThreads), 0, s, logits, vocab, jobs, sampled);
   if (e != cudaSuccess) return e;
   return launch_walk_batched(token, parent, sampled, batch, node_offset, vocab, prefix, m, path,
                              out_tokens, new_pos, new_parent, n_survivors, dev_status, s);

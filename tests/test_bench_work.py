@@ -34,7 +34,7 @@ def test_star_tree_counts():
 
 def test_bounds_scale_with_their_peaks():
     peaks = {"hbm_gbs": 1000.0, "bf16_tflops": 100.0, "sm_max_mhz": 1000.0}
-    b = bench._bounds_us(2e9, 3e12, 152 * 16 * 1e9, peaks)
+    b = bench._bounds_us(2e9, 3e12, 152 * 16 * 1e9, peaks, sms=152)
     assert abs(b["hbm"] - 2000.0) < 1e-9
     assert abs(b["tensor"] - 30000.0) < 1e-9
     assert abs(b["exp"] - 1e6) < 1e-6
