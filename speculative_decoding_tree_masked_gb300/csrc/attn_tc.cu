@@ -105,6 +105,7 @@ struct TcParams {
   int32_t* dev_status;
   int32_t n, hq, hkv, prefix, keys, keys_per_split, splits, rows_per_head;
   int32_t q_tma;  // 1: Q tiles arrive by TMA (G divides 128), 0: threads gather them
+  int32_t tiles_per_cta;  // 128-row tiles of one row group (1 or 2)
   float scale_log2;
   // paged K/V (null: one contiguous cache per KV head): logical key row r
   // is row r % page_size of page page_table[r / page_size] of the pool
@@ -254,8 +255,8 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.hq / p.hkv;
-  const int row0 = rgroup * (kTiles * kBM);
-  const int ntiles = min(kTiles, (p.rows_per_head - row0 + kBM - 1) / kBM);
+  const int row0 = rgroup * (p.tiles_per_cta * kBM);
+  const int ntiles = min(p.tiles_per_cta, (p.rows_per_head - row0 + kBM - 1) / kBM);
   const int kbeg = split * p.keys_per_split;
   const int kend = min(p.keys, kbeg + p.keys_per_split);
   const int nb = (kend - kbeg + kBN - 1) / kBN;
@@ -997,6 +998,7 @@ bool fill_request(const AttnProblem& p, const SplitPlan& plan, float* ws, CUtens
   tp->prefix = p.prefix;
   tp->keys = rows;
   tp->keys_per_split = plan.keys_per_split;
+  tp->tiles_per_cta = plan.tiles_per_cta;
   tp->splits = plan.splits;
   tp->rows_per_head = (p.hq / p.hkv) * p.n;
   tp->scale_log2 = p.scale_log2;

@@ -66,7 +66,8 @@ constexpr int kMaxPageSlots = 1024;
 // Split-KV plan: key range [0, P + N) cut into `splits` chunks of
 // `keys_per_split` keys (a multiple of the kernel's key block).
 struct SplitPlan {
-  int32_t row_tiles;       // tiles of rows per KV head
+  int32_t row_tiles;       // row groups per KV head (CTAs along the rows)
+  int32_t tiles_per_cta;   // 128-row tiles per row group (tensor-core kernel: 1 or 2)
   int32_t splits;
   int32_t keys_per_split;
   size_t ws_bytes;         // partial O + row max + row sum

@@ -327,10 +327,14 @@ def test_attention_plan_is_host_only_and_consistent(lib):
     import speculative_decoding_tree_masked_gb300 as tvp
     # the full verify step's layer on GB300's 152 SMs: two row groups of two
     # 128-row tiles per KV head, 9 splits of 4 key blocks (the last holds the
-    # tree block), fp16 partials
+    # tree block), bf16 partials
     assert tvp.attn_plan(64, 64, 8, 128, torch.bfloat16, 4096, sm_count=152) == {
         "row_groups": 2, "splits": 9, "keys_per_split": 512,
         "ws_bytes": 9 * 4096 * 4 + 9 * 4096 * 128 * 2}
+    # 32 nodes of 8 heads: two tiles per KV head, one per CTA, 9 splits
+    assert tvp.attn_plan(32, 64, 8, 128, torch.bfloat16, 4096, sm_count=152) == {
+        "row_groups": 2, "splits": 9, "keys_per_split": 512,
+        "ws_bytes": 9 * 2048 * 4 + 9 * 2048 * 128 * 2}
     shapes = [(64, 8), (32, 8), (4, 1), (7, 1)]
     for (hq, hkv), n, d, P, sms in itertools.product(shapes, (1, 8, 33, 64, 128), (64, 128),
                                                      (0, 1, 127, 1024, 4096, 32768, 100000),
@@ -340,7 +344,7 @@ def test_attention_plan_is_host_only_and_consistent(lib):
         assert p["keys_per_split"] % 128 == 0
         assert (p["splits"] - 1) * p["keys_per_split"] < keys <= p["splits"] * p["keys_per_split"]
         tiles = -(-(hq // hkv) * n // 128)
-        assert p["row_groups"] == (1 if tiles <= 1 else (tiles + 1) // 2)
+        assert p["row_groups"] == (tiles if tiles <= 2 else (tiles + 1) // 2)
         units = hkv * p["row_groups"]
         assert units * p["splits"] <= max(sms, units)        # one wave of one-CTA-per-SM
         if sms == 256:                                       # the no-device workspace bound
