@@ -152,9 +152,11 @@ template <typename PT, typename T, int D, int S>
 __global__ void __launch_bounds__(256) combine_kernel(const uint8_t* __restrict__ ws, int splits,
                                                       int rows, T* __restrict__ out) {
   constexpr int C = D / 32;  // consecutive columns per lane
-  // the next layer's attention kernel (launched under programmatic
-  // serialization) may start its setup now; it waits for this grid to
-  // finish before it reads or writes memory
+  // launched under programmatic serialization: wait for the attention
+  // kernel that writes the partials; only then let the next layer's
+  // attention kernel start its setup (it waits for this grid to finish
+  // before it reads or writes memory)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -203,9 +205,23 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint8_t* __restrict_
   for (int c = 0; c < C; ++c) store_f32(dst + c, o[c] * inv);
 }
 
+// A combine grid of at most one CTA per SM is launched under programmatic
+// serialization: its CTAs wait, one beside each attention CTA, while the
+// attention kernel finishes (the attention kernel signals once its products
+// are done), which hides its launch.  A larger grid is launched normally:
+// its waiting CTAs crowded the attention's SMs (measured slower).
+bool combine_launches_early(int rows) {
+  const int sms = device_sm_count();
+  return sms > 0 && (rows + 7) / 8 <= sms;
+}
+
 template <typename PT, typename T, int D, int S>
 void launch_combine_s(const uint8_t* w, int splits, int rows, T* out, cudaStream_t s) {
-  combine_kernel<PT, T, D, S><<<(rows + 7) / 8, 256, 0, s>>>(w, splits, rows, out);
+  const dim3 grid((rows + 7) / 8);
+  if (combine_launches_early(rows))
+    launch_pdl(combine_kernel<PT, T, D, S>, grid, dim3(256), 0, s, w, splits, rows, out);
+  else
+    combine_kernel<PT, T, D, S><<<grid, 256, 0, s>>>(w, splits, rows, out);
 }
 
 template <typename PT, typename T, int D>

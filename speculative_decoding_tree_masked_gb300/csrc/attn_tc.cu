@@ -105,6 +105,7 @@ struct TcParams {
   int32_t* dev_status;
   int32_t n, hq, hkv, prefix, keys, keys_per_split, splits, rows_per_head;
   int32_t q_tma;  // 1: Q tiles arrive by TMA (G divides 128), 0: threads gather them
+  int32_t signal_combine;  // 1: a combine launched early follows this kernel
   int32_t tiles_per_cta;  // 128-row tiles of one row group (1 or 2)
   float scale_log2;
   // paged K/V (null: one contiguous cache per KV head): logical key row r
@@ -726,6 +727,12 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
       }
       // epilogue: O_t is final once the last PV has completed
       if (ok) ok = wait_bar(bars.o_final(t), 0, abort_flag, p.dev_status);
+      // every product of the CTA is done once its last tile's O is final:
+      // the combine, launched behind this kernel under programmatic
+      // serialization, may be scheduled now (it waits for this grid before
+      // reading)
+      if (p.signal_combine && t == ntiles - 1 && (sw & 3) == 0 && lane == 0)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
       // Every product of the CTA is done once the last tile's O is final: a
       // kernel launched after this one under programmatic serialization (the
       // combine of the splits) may be scheduled now; it waits for this grid
@@ -998,6 +1005,7 @@ bool fill_request(const AttnProblem& p, const SplitPlan& plan, float* ws, CUtens
   tp->prefix = p.prefix;
   tp->keys = rows;
   tp->keys_per_split = plan.keys_per_split;
+  tp->signal_combine = plan.splits > 1 && combine_launches_early(p.n * p.hq) ? 1 : 0;
   tp->tiles_per_cta = plan.tiles_per_cta;
   tp->splits = plan.splits;
   tp->rows_per_head = (p.hq / p.hkv) * p.n;

@@ -107,6 +107,9 @@ cudaError_t launch_attn_tc_batched(const AttnProblem* probs, const SplitPlan* pl
                                    int batch_n, float* const* ws, cudaStream_t s);
 cudaError_t launch_combine(const AttnProblem& p, const SplitPlan& plan, const float* ws,
                            cudaStream_t s);
+// Whether the combine of an attention with this many output rows (N * Hq)
+// is launched under programmatic serialization right behind the kernel.
+bool combine_launches_early(int rows);
 
 cudaError_t launch_tree_mask(const int32_t* parent, int32_t n, uint32_t* words,
                              int32_t* dev_status, cudaStream_t s);
