@@ -145,10 +145,13 @@ __device__ __forceinline__ void load_partial(const __nv_bfloat16* p, float (&o)[
 }
 
 // One warp per output row: O = sum_s 2^(lse_s - M) O_s / sum_s 2^(lse_s - M).
-// The merge is latency-bound: with the split count S known at compile time a
-// warp keeps all S partial loads in flight at once (one round trip for the
-// log-sum-exps, one for the partial rows); other split counts take the loop.
-template <typename PT, typename T, int D, int S>
+// The merge is latency-bound, so every load of a row is issued before any is
+// used: with the split count S known at compile time a warp keeps all S
+// partial loads in flight at once; otherwise (SMAX > 0) lane s holds split
+// s's log-sum-exp, the maximum and the sum come from warp shuffles, and the
+// partial loads of up to SMAX splits are issued together with it (one round
+// trip in all); beyond 32 splits the loop takes one split at a time.
+template <typename PT, typename T, int D, int S, int SMAX>
 __global__ void __launch_bounds__(256) combine_kernel(const uint8_t* __restrict__ ws, int splits,
                                                       int rows, T* __restrict__ out) {
   constexpr int C = D / 32;  // consecutive columns per lane
@@ -184,6 +187,47 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint8_t* __restrict_
 #pragma unroll
       for (int c = 0; c < C; ++c) o[c] = fmaf(w, x[s][c], o[c]);
     }
+  } else if constexpr (SMAX > 0) {
+    // bf16 partials stay packed (two to a register) until they are used
+    static_assert(sizeof(PT) == 2 && C % 2 == 0, "packed loads take bf16 partials");
+    constexpr int P2 = C / 2;  // 32-bit words per lane and split
+    const float ls = lane < splits ? __ldg(lse + (size_t)lane * rows + row) : -INFINITY;
+    uint32_t raw[SMAX][P2];
+#pragma unroll
+    for (int s = 0; s < SMAX; ++s) {
+      const uint32_t* src =
+          reinterpret_cast<const uint32_t*>(po + ((size_t)s * rows + row) * D + lane * C);
+      if (s < splits) {
+        if constexpr (P2 == 2) {
+          const uint2 v = __ldg(reinterpret_cast<const uint2*>(src));
+          raw[s][0] = v.x;
+          raw[s][1] = v.y;
+        } else {
+#pragma unroll
+          for (int k = 0; k < P2; ++k) raw[s][k] = __ldg(src + k);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < P2; ++k) raw[s][k] = 0u;
+      }
+    }
+    float M = ls;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float w_mine = (ls == -INFINITY) ? 0.f : exp2f(ls - M);
+    W = w_mine;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+#pragma unroll
+    for (int s = 0; s < SMAX; ++s) {
+      const float w = __shfl_sync(0xffffffffu, w_mine, s);  // 0 for s >= splits
+#pragma unroll
+      for (int k = 0; k < P2; ++k) {
+        // a bf16 value is the top half of the float32 with the same bits
+        o[2 * k] = fmaf(w, __uint_as_float(raw[s][k] << 16), o[2 * k]);
+        o[2 * k + 1] = fmaf(w, __uint_as_float(raw[s][k] & 0xffff0000u), o[2 * k + 1]);
+      }
+    }
   } else {
     float M = -INFINITY;
 #pragma unroll 4
@@ -215,13 +259,13 @@ bool combine_launches_early(int rows) {
   return sms > 0 && (rows + 7) / 8 <= sms;
 }
 
-template <typename PT, typename T, int D, int S>
+template <typename PT, typename T, int D, int S, int SMAX = 0>
 void launch_combine_s(const uint8_t* w, int splits, int rows, T* out, cudaStream_t s) {
   const dim3 grid((rows + 7) / 8);
   if (combine_launches_early(rows))
-    launch_pdl(combine_kernel<PT, T, D, S>, grid, dim3(256), 0, s, w, splits, rows, out);
+    launch_pdl(combine_kernel<PT, T, D, S, SMAX>, grid, dim3(256), 0, s, w, splits, rows, out);
   else
-    combine_kernel<PT, T, D, S><<<grid, 256, 0, s>>>(w, splits, rows, out);
+    combine_kernel<PT, T, D, S, SMAX><<<grid, 256, 0, s>>>(w, splits, rows, out);
 }
 
 template <typename PT, typename T, int D>
@@ -233,7 +277,11 @@ void launch_combine_d(const uint8_t* w, int splits, int rows, T* out, cudaStream
     TV_COMBINE_CASE(6) TV_COMBINE_CASE(7) TV_COMBINE_CASE(8) TV_COMBINE_CASE(9)
     TV_COMBINE_CASE(10) TV_COMBINE_CASE(11) TV_COMBINE_CASE(12)
 #undef TV_COMBINE_CASE
-    default: launch_combine_s<PT, T, D, 0>(w, splits, rows, out, s); break;
+    default:
+      if (splits <= 16) launch_combine_s<PT, T, D, 0, 16>(w, splits, rows, out, s);
+      else if (splits <= 32) launch_combine_s<PT, T, D, 0, 32>(w, splits, rows, out, s);
+      else launch_combine_s<PT, T, D, 0>(w, splits, rows, out, s);
+      break;
   }
 }
 
