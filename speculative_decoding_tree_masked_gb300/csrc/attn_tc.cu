@@ -94,8 +94,6 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr long long kWaitCycles = 4000000000LL;
 constexpr uint32_t kSleepHintNs = 20000;  // longest single hardware sleep of a wait
-// A/B switch: where dependents are signalled (0 after the last product, 1 after the output store)
-constexpr int kTriggerAt = 0;
 
 struct TcParams {
   const __nv_bfloat16* q;
@@ -733,12 +731,6 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
       // reading)
       if (p.signal_combine && t == ntiles - 1 && (sw & 3) == 0 && lane == 0)
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-      // Every product of the CTA is done once the last tile's O is final: a
-      // kernel launched after this one under programmatic serialization (the
-      // combine of the splits) may be scheduled now; it waits for this grid
-      // to complete before it reads anything.  One thread signals.
-      if (kTriggerAt == 0 && t == ntiles - 1 && (sw & 3) == 0 && lane == 0)
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
       // Stage this thread's normalised row as 16-bit values in shared memory
       // (the Q tiles are free: every MMA has completed), then copy the tile
       // out.  With one split the result is the final bf16 output; otherwise
@@ -835,7 +827,6 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
     }
   }
 
-  if (kTriggerAt == 1 && tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   ptx::tc_fence_before();
   __syncthreads();
   if (*abort_flag) {
