@@ -208,3 +208,19 @@ def test_single_tile_with_late_maxima(grow):
     out = _run(q, k, v, P, parent)
     nodes = [0, 3, 7]
     assert _err(out, _ref(q, k, v, P, parent, nodes=nodes), nodes) <= BF16_TOL
+
+
+@pytest.mark.parametrize("hq,hkv,n,P,lo,hi", [
+    (64, 8, 64, 4096, 2, 12),      # per-count combine (9 splits at the full step's layer)
+    (64, 8, 8, 8192, 13, 32),      # lane-parallel combine: 17 splits of a short tree
+    (8, 1, 8, 8192, 33, 10 ** 6),  # one KV head: more than 32 splits, the loop
+])
+def test_each_combine_path(hq, hkv, n, P, lo, hi):
+    splits = tvp.attn_plan(n, hq, hkv, 128, torch.bfloat16, P)["splits"]
+    assert lo <= splits <= hi, splits
+    rng = np.random.default_rng(900 + splits)
+    parent = synth.random_parent_tree(rng, n, max_depth=8)
+    q, k, v = _qkv(rng, n, hq, hkv, 128, P + n, torch.bfloat16)
+    out = _run(q, k, v, P, parent)
+    nodes = sorted({0, n // 2, n - 1})
+    assert _err(out, _ref(q, k, v, P, parent, nodes=nodes), nodes) <= BF16_TOL
