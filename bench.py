@@ -879,8 +879,12 @@ def run_sweep(args, local_rank):
     stream = torch.cuda.Stream(dev)
     peaks = _peaks()
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    nmax = max(SWEEP_NODES)
-    for prefix in SWEEP_PREFIXES:
+    prefixes = tuple(int(x) for x in args.sweep_prefix.split(",")) if args.sweep_prefix \
+        else SWEEP_PREFIXES
+    nodes = tuple(int(x) for x in args.sweep_nodes.split(",")) if args.sweep_nodes \
+        else SWEEP_NODES
+    nmax = max(nodes)
+    for prefix in prefixes:
         big = synth.make_workload("q2_72b", seed=args.seed, prefix=prefix, n=nmax)
         q_all, k0, v0 = synth.make_qkv(big, layer=0)
         k0, v0 = k0.to(dev), v0.to(dev)
@@ -888,7 +892,7 @@ def run_sweep(args, local_rank):
         copies = int(min(96, max(3, -(-3 * 130_000_000 // kv_bytes))))
         ks = [k0] + [k0.clone() for _ in range(copies - 1)]
         vs = [v0] + [v0.clone() for _ in range(copies - 1)]
-        for n in SWEEP_NODES:
+        for n in nodes:
             w = synth.make_workload("q2_72b", seed=args.seed, prefix=prefix, n=n)
             q = q_all[:n].contiguous().to(dev)
             parent = torch.from_numpy(w.parent).to(dev)
@@ -1374,6 +1378,10 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="time the attention alone over the prefix x tree-size sweep "
                          "(one JSON line per configuration) instead of the step")
+    ap.add_argument("--sweep-prefix", default="",
+                    help="with --sweep: comma-separated prefix lengths (default: the full sweep)")
+    ap.add_argument("--sweep-nodes", default="",
+                    help="with --sweep: comma-separated tree sizes (default: the full sweep)")
     ap.add_argument("--sdpa", action="store_true",
                     help="with --sweep: also time PyTorch's SDPA on the same inputs (context)")
     ap.add_argument("--no-configs", action="store_true",

@@ -329,6 +329,7 @@ expand_merge_kernel(const float* __restrict__ ws, int nf, int chunks, int w,
   __shared__ int s_key[kRowCands];
   __shared__ float o_s[TV_MAX_EXPAND_WIDTH];
   __shared__ int o_k[TV_MAX_EXPAND_WIDTH];
+  __shared__ int s_front[kRowCands];     // each row's frontier node (nf <= 1024)
   __shared__ int s_bad;
   // launched under programmatic serialization after the slice kernel
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -345,6 +346,23 @@ expand_merge_kernel(const float* __restrict__ ws, int nf, int chunks, int w,
   for (int f = warp; f < nf; f += kMergeThreads / 32) {
     const float* rows = ws + (size_t)f * chunks * rw;
     const int total = chunks * w;
+    // Every global read of the row is requested before any is waited for,
+    // so that the row costs about two L2 round trips rather than five: the
+    // frontier node first (its path score is a dependent load), then the
+    // slice maxima and sums (rows of up to 128 slices; longer ones take a
+    // second pass below) and the slice candidates.
+    const int u = frontier[f];
+    const bool u_ok = u >= 0 && u < n_nodes;
+    const bool one_pass = chunks <= 128;
+    float rm1[4], rs1[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int cc = lane + 32 * q;
+      const bool on = one_pass && cc < chunks;
+      rm1[q] = on ? rows[(size_t)cc * rw] : -INFINITY;
+      rs1[q] = on ? rows[(size_t)cc * rw + 1] : 0.f;
+    }
+    float base = 0.f;
     // staged 32 loads per lane at a time (all of them when chunks * w <= 1024),
     // all issued before any is stored
     for (int o0 = 0; o0 < total; o0 += 32 * 32) {
@@ -358,6 +376,7 @@ expand_merge_kernel(const float* __restrict__ ws, int nf, int chunks, int w,
         zv[q] = rec[2 + 2 * k];
         tv[q] = reinterpret_cast<const int*>(rec)[3 + 2 * k];
       }
+      if (o0 == 0 && u_ok) base = cum[u];
 #pragma unroll
       for (int q = 0; q < 32; ++q) {
         const int o = o0 + lane + 32 * q;
@@ -368,9 +387,9 @@ expand_merge_kernel(const float* __restrict__ ws, int nf, int chunks, int w,
       }
     }
     // log-sum-exp: M = max m_c, S = sum s_c e^(m_c - M), four slice records
-    // per lane loaded together
-    float m = -INFINITY;
-    for (int c0 = 0; c0 < chunks; c0 += 128) {
+    // per lane at a time
+    float m = one_pass ? fmaxf(fmaxf(rm1[0], rm1[1]), fmaxf(rm1[2], rm1[3])) : -INFINITY;
+    for (int c0 = 0; !one_pass && c0 < chunks; c0 += 128) {
       float rm[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -382,8 +401,13 @@ expand_merge_kernel(const float* __restrict__ ws, int nf, int chunks, int w,
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float sum = 0.f;
-    if (m != -INFINITY)
-      for (int c0 = 0; c0 < chunks; c0 += 128) {
+    if (m != -INFINITY) {
+      if (one_pass) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (rm1[q] != -INFINITY) sum += rs1[q] * __expf(rm1[q] - m);
+      }
+      for (int c0 = 0; !one_pass && c0 < chunks; c0 += 128) {
         float rm[4], rs[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -395,13 +419,14 @@ expand_merge_kernel(const float* __restrict__ ws, int nf, int chunks, int w,
         for (int q = 0; q < 4; ++q)
           if (rm[q] != -INFINITY) sum += rs[q] * __expf(rm[q] - m);
       }
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     const float lse = m + __logf(sum);
-    const int u = frontier[f];
-    const bool u_ok = u >= 0 && u < n_nodes;
-    if (!u_ok && lane == 0) s_bad = 1;
-    const float base = u_ok ? cum[u] : 0.f;
+    if (lane == 0) {
+      s_front[f] = u;
+      if (!u_ok) s_bad = 1;
+    }
     __syncwarp();
     warp_kmerge(zl, tl, chunks, w, w, w, s_sc + f * w, s_key + f * w);
     __syncwarp();
@@ -429,7 +454,7 @@ expand_merge_kernel(const float* __restrict__ ws, int nf, int chunks, int w,
     __syncwarp();
     for (int k = lane; k < w; k += 32) {
       const int kk = o_k[k];
-      new_parent[k] = kk >= 0 ? frontier[kk >> 20] : -1;
+      new_parent[k] = kk >= 0 ? s_front[kk >> 20] : -1;
       new_token[k] = kk >= 0 ? (kk & 0xfffff) : -1;
       new_score[k] = kk >= 0 ? o_s[k] : -INFINITY;
     }
