@@ -249,39 +249,39 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint8_t* __restrict_
   for (int c = 0; c < C; ++c) store_f32(dst + c, o[c] * inv);
 }
 
-// A combine grid of at most one CTA per SM is launched under programmatic
-// serialization: its CTAs wait, one beside each attention CTA, while the
-// attention kernel finishes (the attention kernel signals once its products
-// are done), which hides its launch.  A larger grid is launched normally:
-// its waiting CTAs crowded the attention's SMs (measured slower).
+// The combine is launched under programmatic serialization and waits for
+// the attention grid before reading.  A grid of at most one CTA per SM is
+// released early: the attention kernel signals once its products are done,
+// and the combine's CTAs wait, one beside each attention CTA, which hides
+// its launch.  A larger grid is released only as the attention CTAs exit
+// (their implicit signal): its CTAs would crowd the attention's SMs while
+// waiting, but it still starts without waiting for the attention grid's
+// completion and flush (0.7-3% faster than a plain launch, measured).
 bool combine_launches_early(int rows) {
   const int sms = device_sm_count();
   return sms > 0 && (rows + 7) / 8 <= sms;
 }
 
 template <typename PT, typename T, int D, int S, int SMAX = 0>
-void launch_combine_s(const uint8_t* w, int splits, int rows, T* out, cudaStream_t s) {
+cudaError_t launch_combine_s(const uint8_t* w, int splits, int rows, T* out, cudaStream_t s) {
   const dim3 grid((rows + 7) / 8);
-  if (combine_launches_early(rows))
-    launch_pdl(combine_kernel<PT, T, D, S, SMAX>, grid, dim3(256), 0, s, w, splits, rows, out);
-  else
-    combine_kernel<PT, T, D, S, SMAX><<<grid, 256, 0, s>>>(w, splits, rows, out);
+  return launch_pdl(combine_kernel<PT, T, D, S, SMAX>, grid, dim3(256), 0, s, w, splits, rows,
+                    out);
 }
 
 template <typename PT, typename T, int D>
-void launch_combine_d(const uint8_t* w, int splits, int rows, T* out, cudaStream_t s) {
+cudaError_t launch_combine_d(const uint8_t* w, int splits, int rows, T* out, cudaStream_t s) {
   switch (splits) {
 #define TV_COMBINE_CASE(n) \
-  case n: launch_combine_s<PT, T, D, n>(w, splits, rows, out, s); break;
+  case n: return launch_combine_s<PT, T, D, n>(w, splits, rows, out, s);
     TV_COMBINE_CASE(2) TV_COMBINE_CASE(3) TV_COMBINE_CASE(4) TV_COMBINE_CASE(5)
     TV_COMBINE_CASE(6) TV_COMBINE_CASE(7) TV_COMBINE_CASE(8) TV_COMBINE_CASE(9)
     TV_COMBINE_CASE(10) TV_COMBINE_CASE(11) TV_COMBINE_CASE(12)
 #undef TV_COMBINE_CASE
     default:
-      if (splits <= 16) launch_combine_s<PT, T, D, 0, 16>(w, splits, rows, out, s);
-      else if (splits <= 32) launch_combine_s<PT, T, D, 0, 32>(w, splits, rows, out, s);
-      else launch_combine_s<PT, T, D, 0>(w, splits, rows, out, s);
-      break;
+      if (splits <= 16) return launch_combine_s<PT, T, D, 0, 16>(w, splits, rows, out, s);
+      if (splits <= 32) return launch_combine_s<PT, T, D, 0, 32>(w, splits, rows, out, s);
+      return launch_combine_s<PT, T, D, 0>(w, splits, rows, out, s);
   }
 }
 
@@ -291,15 +291,14 @@ cudaError_t launch_combine(const AttnProblem& p, const SplitPlan& plan, const fl
   const auto* w = reinterpret_cast<const uint8_t*>(ws);
   if (p.dtype == TV_BF16) {
     auto* out = static_cast<__nv_bfloat16*>(p.out);
-    if (p.d == 128) launch_combine_d<__nv_bfloat16, __nv_bfloat16, 128>(w, plan.splits, rows, out, s);
-    else launch_combine_d<__nv_bfloat16, __nv_bfloat16, 64>(w, plan.splits, rows, out, s);
-  } else {
-    // the fp32 path is not latency-critical: one loop kernel
-    auto* out = static_cast<float*>(p.out);
-    if (p.d == 128) launch_combine_s<float, float, 128, 0>(w, plan.splits, rows, out, s);
-    else launch_combine_s<float, float, 64, 0>(w, plan.splits, rows, out, s);
+    return p.d == 128
+               ? launch_combine_d<__nv_bfloat16, __nv_bfloat16, 128>(w, plan.splits, rows, out, s)
+               : launch_combine_d<__nv_bfloat16, __nv_bfloat16, 64>(w, plan.splits, rows, out, s);
   }
-  return cudaGetLastError();
+  // the fp32 path is not latency-critical: one loop kernel
+  auto* out = static_cast<float*>(p.out);
+  return p.d == 128 ? launch_combine_s<float, float, 128, 0>(w, plan.splits, rows, out, s)
+                    : launch_combine_s<float, float, 64, 0>(w, plan.splits, rows, out, s);
 }
 
 }  // namespace tv
