@@ -332,15 +332,26 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
   // to land before the CTA exits.
   int k_last = -1, v_last = -1;  // last K and V block requested
   bool q_requested = false;
+  // With two tiles, K(j + 1) lands on V(j)'s barrier, armed for both copies
+  // (one wait per block for the MMA thread), except K(2), which waits for
+  // block 0's products and so keeps its own barrier: no armed phase may wait
+  // on anything but copies already requested.
+  const bool kv_pair = !db;
+  auto paired_k = [&](int j) { return kv_pair && j >= 1 && j != kStages; };
   auto load_k = [&](int j) {
     const int s = j % kStages;
-    ptx::mbar_arrive_expect_tx(bars.k_full(s), L::kKV);
-    load_block(kmap, base + L::kK + s * L::kKV, bars.k_full(s), j, j == 0);
+    if (paired_k(j)) {
+      load_block(kmap, base + L::kK + s * L::kKV, bars.v_full((j - 1) % kStages), j, j == 0);
+    } else {
+      ptx::mbar_arrive_expect_tx(bars.k_full(s), L::kKV);
+      load_block(kmap, base + L::kK + s * L::kKV, bars.k_full(s), j, j == 0);
+    }
     k_last = j;
   };
   auto load_v = [&](int j) {
     const int s = j % kStages;
-    ptx::mbar_arrive_expect_tx(bars.v_full(s), L::kKV);
+    const bool pair = j + 1 < nb && paired_k(j + 1);
+    ptx::mbar_arrive_expect_tx(bars.v_full(s), pair ? 2 * L::kKV : L::kKV);
     load_block(vmap, base + L::kV + s * L::kKV, bars.v_full(s), j, false);
     v_last = j;
   };
@@ -448,8 +459,8 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
       // QK^T of every CTA is fed ahead of everything else.  After that a
       // slot is refilled once the last product reading it is done: with two
       // tiles, block j's single release frees V slot j % 2 and K slot
-      // (j + 1) % 2, for V(j + 2) and K(j + 3); keys run about half a block
-      // ahead of values.
+      // (j + 1) % 2, for V(j + 2) and K(j + 3), which land on one barrier;
+      // keys run about half a block ahead of values.
       if (db) {
         // double-buffered scores: QK^T runs a block ahead of PV, so keys are
         // requested a block ahead of values (K_0, K_1, V_0, K_2, V_1, ...)
@@ -582,7 +593,8 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
         const bool more = j + 1 < nb;
         const int s2 = (j + 1) % kStages, u2 = (j + 1) / kStages;
         ok = wait_bar(bars.v_full(s), u & 1, abort_flag, p.dev_status);
-        if (ok && more) ok = wait_bar(bars.k_full(s2), u2 & 1, abort_flag, p.dev_status);
+        if (ok && more && j + 1 == kStages)
+          ok = wait_bar(bars.k_full(s2), u2 & 1, abort_flag, p.dev_status);
         for (int t = 0; t < ntiles && ok; ++t) {
           ok = wait_bar(bars.p_full(t), j & 1, abort_flag, p.dev_status);
           if (!ok) break;
@@ -820,8 +832,12 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
     if (tid == 0) {
       for (int s = 0; s < kStages; ++s) {
         // the last block requested into slot s is the newest phase there
+        // (with two tiles K(0) and K(2) use k_full(0); every other K(j)
+        // completes within V(j - 1)'s phase, awaited below)
         const int jk = k_last - ((k_last - s) % kStages + kStages) % kStages;
-        if (k_last >= 0 && jk >= 0) drain_wait(bars.k_full(s), (jk / kStages) & 1, p.dev_status);
+        const int jk_own = !kv_pair ? jk : (s == 0 ? (k_last >= kStages ? kStages : 0) : -1);
+        if (k_last >= 0 && jk_own >= 0)
+          drain_wait(bars.k_full(s), (jk_own / kStages) & 1, p.dev_status);
         const int jv = v_last - ((v_last - s) % kStages + kStages) % kStages;
         if (v_last >= 0 && jv >= 0) drain_wait(bars.v_full(s), (jv / kStages) & 1, p.dev_status);
       }
