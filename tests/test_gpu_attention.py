@@ -224,3 +224,25 @@ def test_each_combine_path(hq, hkv, n, P, lo, hi):
     out = _run(q, k, v, P, parent)
     nodes = sorted({0, n // 2, n - 1})
     assert _err(out, _ref(q, k, v, P, parent, nodes=nodes), nodes) <= BF16_TOL
+
+
+# Key blocks per CTA: with two tiles per CTA (N 64) V(j) and K(j+1) share a
+# barrier except K(2); with one tile (N 32, N 8) the K slot release is read
+# from the score barrier.  Each case pins the split plan so that CTAs hold 1 to
+# 8 key blocks (the last split often fewer), covering every pairing edge.
+@pytest.mark.parametrize("n,P,per", [
+    (64, 500, 1), (64, 1500, 2), (64, 3000, 3), (64, 5000, 5), (64, 6000, 6),
+    (32, 1200, 2), (32, 2500, 3), (32, 3500, 4), (32, 9000, 8), (8, 2500, 2), (8, 9000, 4),
+])
+def test_blocks_per_cta(n, P, per):
+    plan = tvp.attn_plan(n, 64, 8, 128, torch.bfloat16, P)
+    assert plan["keys_per_split"] // 128 == per, plan
+    rng = np.random.default_rng(700 + n + P)
+    parent = synth.random_parent_tree(rng, n, max_depth=8)
+    q, k, v = _qkv(rng, n, 64, 8, 128, P + n, torch.bfloat16)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _run(q, k, v, P, parent, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    nodes = sorted({0, n // 3, n - 1})
+    assert _err(out, _ref(q, k, v, P, parent, nodes=nodes), nodes) <= BF16_TOL
