@@ -246,3 +246,18 @@ def test_blocks_per_cta(n, P, per):
     assert int(st.item()) == 0
     nodes = sorted({0, n // 3, n - 1})
     assert _err(out, _ref(q, k, v, P, parent, nodes=nodes), nodes) <= BF16_TOL
+
+
+# The d 64 instantiation of the tensor-core kernel at the full step's head
+# layout: two tiles per CTA (N 64) and one (N 32, N 8), several key blocks each.
+@pytest.mark.parametrize("n,P", [(64, 3000), (64, 600), (32, 2500), (8, 9000)])
+def test_head_dim_64_tile_paths(n, P):
+    rng = np.random.default_rng(1100 + n + P)
+    parent = synth.random_parent_tree(rng, n, max_depth=8)
+    q, k, v = _qkv(rng, n, 64, 8, 64, P + n, torch.bfloat16)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _run(q, k, v, P, parent, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    nodes = sorted({0, n // 2, n - 1})
+    assert _err(out, _ref(q, k, v, P, parent, nodes=nodes), nodes) <= BF16_TOL
