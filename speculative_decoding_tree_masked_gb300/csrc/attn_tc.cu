@@ -538,7 +538,9 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
       if (db) {
         // one tile, scores in two buffers: QK^T(j + 2) is issued right after
         // PV(j) has freed buffer j % 2; MMAs from one thread run in order, so
-        // PV(j) reads P before QK^T overwrites it
+        // PV(j) reads P before QK^T overwrites it.  Two commits per block:
+        // the V slot release (also the softmax's sign that PV(j) is done) and
+        // the scores of block j + 2 (also the release of K slot j % 2).
         if (ok) {
           ptx::tc_fence_after();
           issue_qk_to(0, 0, 0);
@@ -583,17 +585,17 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
       }
       // The tensor pipe queues only a few MMAs and every barrier operation
       // of this thread costs tens of cycles, so none sits between a tile's
-      // PV and QK^T: V of this block and K of the next are waited for at the
-      // top of the block (in this compute-bound path they have landed), the
-      // products of a tile then issue back to back, and one commit per block
-      // releases both slots.  (Each barrier operation taken out of the
-      // product stream measured 1-2% at N >= 64.)
+      // PV and QK^T: V of this block and K of the next (one barrier, but for
+      // K(2)) are waited for at the top of the block (in this compute-bound
+      // path they have landed), the products of a tile then issue back to
+      // back, and one commit per block releases both slots.  (Each barrier
+      // operation taken out of the product stream measured 1-2% at N >= 64.)
       for (int j = 0; ok && j < nb; ++j) {
         const int s = j % kStages, u = j / kStages;
         const bool more = j + 1 < nb;
         const int s2 = (j + 1) % kStages, u2 = (j + 1) / kStages;
         ok = wait_bar(bars.v_full(s), u & 1, abort_flag, p.dev_status);
-        if (ok && more && j + 1 == kStages)
+        if (ok && more && j + 1 == kStages)  // K(2) has its own barrier
           ok = wait_bar(bars.k_full(s2), u2 & 1, abort_flag, p.dev_status);
         for (int t = 0; t < ntiles && ok; ++t) {
           ok = wait_bar(bars.p_full(t), j & 1, abort_flag, p.dev_status);
@@ -696,8 +698,9 @@ attn_tc_kernel(const __grid_constant__ TcBatch<MAXB> batch) {
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
           // O_t must hold the sum through block j-1.  With one buffer per
           // tile, S_t(j) complete implies PV_t(j-1) complete (see above);
-          // with double-buffered scores PV(j-1) may still run: wait for it.
-          // PV_t(j) waits for this thread's P_full arrival.
+          // with double-buffered scores PV(j-1) may still run: wait for it
+          // (its V slot's release).  PV_t(j) waits for this thread's P_full
+          // arrival.
           if (db && !wait_bar(bars.v_empty((j - 1) % kStages), ((j - 1) / kStages) & 1, abort_flag,
                               p.dev_status))
             ok = false;
