@@ -336,9 +336,11 @@ expand_merge_kernel(const float* __restrict__ ws, int nf, int chunks, int w,
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const size_t rw = record_words(w);
   // o / w as a multiply-high by ceil(2^32 / w): exact for o < 2^16 and
-  // w <= 64 (here o < kRowCands), and free of the long dependent chain of an
-  // integer division
-  const uint32_t w_recip = (uint32_t)((0x100000000ull + (uint64_t)w - 1) / (uint64_t)w);
+  // 2 <= w <= 64 (here o < kRowCands), and free of the long dependent chain
+  // of an integer division.  For w = 1 that multiplier, 2^32, does not fit
+  // in 32 bits: the quotient is o itself.
+  const uint32_t w_recip =
+      w > 1 ? (uint32_t)((0x100000000ull + (uint64_t)w - 1) / (uint64_t)w) : 0u;
   float* zl = merge_smem + (size_t)warp * 2 * kRowCands;
   int* tl = reinterpret_cast<int*>(zl + kRowCands);
   if (tid == 0) s_bad = 0;
@@ -371,7 +373,7 @@ expand_merge_kernel(const float* __restrict__ ws, int nf, int chunks, int w,
 #pragma unroll
       for (int q = 0; q < 32; ++q) {
         const int o = min(o0 + lane + 32 * q, total - 1);
-        const int cc = (int)__umulhi((uint32_t)o, w_recip), k = o - cc * w;
+        const int cc = w > 1 ? (int)__umulhi((uint32_t)o, w_recip) : o, k = o - cc * w;
         const float* rec = rows + (size_t)cc * rw;
         zv[q] = rec[2 + 2 * k];
         tv[q] = reinterpret_cast<const int*>(rec)[3 + 2 * k];

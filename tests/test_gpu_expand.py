@@ -54,7 +54,10 @@ def _check_expansion(logits, frontier, cum, w, got):
 
 @pytest.mark.parametrize("nf,vocab,w", [(1, 1000, 1), (1, 128256, 8), (8, 128256, 8),
                                         (3, 33, 16), (8, 4099, 64), (128, 997, 8),
-                                        (16, 128256, 64), (5, 1, 5), (2, 524288, 16), (1, 131072, 64)])
+                                        (16, 128256, 64), (5, 1, 5), (2, 524288, 16), (1, 131072, 64),
+                                        # w = 1 over many slices per row (a chain draft)
+                                        (1, 128256, 1), (8, 128256, 1), (64, 128256, 1),
+                                        (3, 5000, 1), (128, 3000, 1)])
 @pytest.mark.parametrize("seed", [0, 1])
 def test_expansion_matches_oracle(nf, vocab, w, seed):
     rng = np.random.default_rng(seed)
