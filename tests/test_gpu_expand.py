@@ -82,6 +82,42 @@ def test_all_equal_scores_follow_the_tie_rule():
     assert got["token"].cpu().tolist() == t.tolist()
 
 
+@pytest.mark.parametrize("w", [1, 8, 64])
+def test_ties_across_slices_and_rows_follow_the_tie_rule(w):
+    # identical rows of 128256 logits with 40 equal maxima spread over the
+    # vocabulary (so over many slices), equal path scores: every pick ties,
+    # and the order is fixed by the frontier position, then the token id
+    rng = np.random.default_rng(w)
+    nf, vocab = 3, 128256
+    row = np.full(vocab, -5.0, dtype=np.float32)
+    row[rng.choice(vocab, size=40, replace=False)] = 2.0
+    logits = np.tile(row, (nf, 1))
+    frontier = np.array([9, 4, 6], dtype=np.int32)
+    cum = np.full(12, -1.5, dtype=np.float32)
+    got = tvp.tree_expand(torch.from_numpy(logits).to(DEV), torch.from_numpy(frontier).to(DEV),
+                          torch.from_numpy(cum).to(DEV), w)
+    p, t, _ = oracle.ml_expand(logits.astype(np.float64), frontier, cum.astype(np.float64), w)
+    assert got["parent"].cpu().tolist() == p.tolist()
+    assert got["token"].cpu().tolist() == t.tolist()
+    sc = got["score"].cpu().numpy()
+    assert (sc == sc[0]).all()                  # the same arithmetic on equal inputs
+
+
+def test_unaligned_logits_rows():
+    # a view that starts one float into a buffer: rows are not 16-byte aligned
+    rng = np.random.default_rng(5)
+    nf, vocab, w = 4, 4096, 8
+    logits = (rng.standard_normal((nf, vocab)) * 3).astype(np.float32)
+    buf = torch.empty(nf * vocab + 1, dtype=torch.float32, device=DEV)
+    buf[1:] = torch.from_numpy(logits.reshape(-1)).to(DEV)
+    frontier = np.array([3, 0, 7, 5], dtype=np.int32)
+    cum = (-rng.uniform(0, 6, size=8)).astype(np.float32)
+    got = tvp.tree_expand(buf[1:].view(nf, vocab), torch.from_numpy(frontier).to(DEV),
+                          torch.from_numpy(cum).to(DEV), w)
+    torch.cuda.synchronize()
+    _check_expansion(logits, frontier, cum, w, got)
+
+
 def test_masked_vocabulary_entries_are_never_preferred():
     rng = np.random.default_rng(3)
     nf, vocab, w = 4, 3000, 8
