@@ -15,9 +15,11 @@
 //                 best, then one warp the best of those.  Within a row the score order
 //                 is the logit order, so the row's best w are among the
 //                 slices' best w.
-//   merge kernel  one CTA: a warp per row turns the row's slice records into
-//                 its log-sum-exp and its w best candidates, then one warp
-//                 picks the w best of all rows by score.
+//   merge kernel  one cluster of up to 8 CTAs (one per 8 rows): a warp per
+//                 row turns the row's slice records into its log-sum-exp
+//                 and its w best candidates; CTA 0 gathers every row's list
+//                 through distributed shared memory and one warp picks the
+//                 w best of all rows by score.
 //
 // Re-rooting (review page, "What carries the argument": the draft tree
 // re-roots at the last verified token and keeps the still-useful subtree):
@@ -28,10 +30,14 @@
 #include <climits>
 #include <cmath>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace tv {
+
+namespace cg = cooperative_groups;
 
 namespace {
 
@@ -42,6 +48,8 @@ constexpr int kChunkWarps = kChunkThreads / 32;
 constexpr int kShortSlice = kChunkThreads * 8;
 constexpr int kMaxChunkLen = kChunkThreads * 32;
 constexpr int kMergeThreads = 256;
+constexpr int kMergeWarps = kMergeThreads / 32;
+constexpr int kMergeCluster = 8;  // merge CTAs at most (a portable cluster)
 constexpr int kRowCands = 1024;  // slice candidates of one row: chunks * w
 
 // A candidate is (value, key): key >= 0 identifies it (a token id, or a
@@ -170,44 +178,52 @@ __device__ __forceinline__ void warp_take8(float (&v)[8], int (&key)[8], int r, 
 // One warp merges nl <= 128 lists held in shared memory, each sorted best
 // first: list l is (vals, keys)[l * stride + 0 .. len), a key < 0 ending it
 // early (keys distinct).  The r best go to out_v / out_k (lane 0 writes).
-// Lane L follows the heads of lists L, L + 32, L + 64 and L + 96, so a round
-// costs a warp reduction and one head step.
+// Lane L follows the heads of lists L, L + 32, L + 64 and L + 96 and holds
+// each list's next entry as well, so a round costs a depth-2 comparison tree,
+// a warp reduction and a register select in the winning lane; the refill of
+// that list's next entry from shared memory is not waited for until the list
+// wins again.
 __device__ __forceinline__ void warp_kmerge(const float* vals, const int* keys, int nl, int len,
                                             int stride, int r, float* out_v, int* out_k) {
   const int lane = threadIdx.x & 31;
-  int head[4] = {0, 0, 0, 0};
-  float hv[4];
-  int hk[4];
+  int head[4];
+  float hv[4], nv[4];
+  int hk[4], nk[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int l = lane + 32 * q;
-    const bool on = l < nl && len > 0;
+    const bool on = l < nl && len > 0, on2 = l < nl && len > 1;
     hv[q] = on ? vals[l * stride] : 0.f;
     hk[q] = on ? keys[l * stride] : -1;
+    nv[q] = on2 ? vals[l * stride + 1] : 0.f;
+    nk[q] = on2 ? keys[l * stride + 1] : -1;
+    head[q] = 1;
   }
   for (int t = 0; t < r; ++t) {
-    float bv = hv[0];
-    int bk = hk[0], bq = 0;
-#pragma unroll
-    for (int q = 1; q < 4; ++q) {
-      const bool b = before(hv[q], hk[q], bv, bk);
-      bv = b ? hv[q] : bv;
-      bk = b ? hk[q] : bk;
-      bq = b ? q : bq;
-    }
+    const bool b1 = before(hv[1], hk[1], hv[0], hk[0]);
+    const bool b3 = before(hv[3], hk[3], hv[2], hk[2]);
+    const float v01 = b1 ? hv[1] : hv[0], v23 = b3 ? hv[3] : hv[2];
+    const int k01 = b1 ? hk[1] : hk[0], k23 = b3 ? hk[3] : hk[2];
+    const bool b = before(v23, k23, v01, k01);
+    const float bv = b ? v23 : v01;
+    const int bk = b ? k23 : k01;
+    const int bq = b ? (b3 ? 3 : 2) : (b1 ? 1 : 0);
     float wv = bv;
     int wk = bk;
     warp_best(wv, wk);
     if (lane == 0) { out_v[t] = wv; out_k[t] = wk; }
-    if (wk >= 0 && wk == bk) {  // this lane's list bq held the winner: step its head
+    const bool won = wk >= 0 && wk == bk;  // this lane's list bq held the winner
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (q != bq) continue;
-        const int l = lane + 32 * q;
+    for (int q = 0; q < 4; ++q) {
+      const bool pop = won && bq == q;
+      hv[q] = pop ? nv[q] : hv[q];
+      hk[q] = pop ? nk[q] : hk[q];
+      if (pop) {
         ++head[q];
+        const int l = lane + 32 * q;
         const bool on = head[q] < len;
-        hv[q] = on ? vals[l * stride + head[q]] : 0.f;
-        hk[q] = on ? keys[l * stride + head[q]] : -1;
+        nv[q] = on ? vals[l * stride + head[q]] : 0.f;
+        nk[q] = on ? keys[l * stride + head[q]] : -1;
       }
     }
   }
@@ -312,11 +328,14 @@ expand_chunk_kernel(const float* __restrict__ logits, int vocab, int chunk_len, 
   }
 }
 
-// One CTA.  Warp f (and f + 8, ...) stages row f's slice lists (each sorted
-// best first) in shared memory, reduces the row's log-sum-exp and merges the
-// lists into the row's w best (the score order within a row is the logit
-// order), then scores them, keyed (f << 20) | token; warp 0 merges the rows'
-// lists by (score, frontier position, token).
+// A grid of ncta <= 8 CTAs launched as one cluster.  Warp f % 8 of CTA
+// (f / 8) % ncta stages row f's slice lists (each sorted best first) in
+// shared memory, reduces the row's log-sum-exp and merges the lists into the
+// row's w best (the score order within a row is the logit order), then
+// scores them, keyed (f << 20) | token.  CTA 0 copies the other CTAs' row
+// lists and frontier nodes into its own arrays (between two cluster
+// barriers, so that no CTA exits while its shared memory is read) and its
+// warp 0 merges the rows' lists by (score, frontier position, token).
 constexpr size_t kMergeSmem = (size_t)(kMergeThreads / 32) * kRowCands * 8;
 
 __global__ void __launch_bounds__(kMergeThreads)
@@ -345,7 +364,8 @@ expand_merge_kernel(const float* __restrict__ ws, int nf, int chunks, int w,
   int* tl = reinterpret_cast<int*>(zl + kRowCands);
   if (tid == 0) s_bad = 0;
   __syncthreads();
-  for (int f = warp; f < nf; f += kMergeThreads / 32) {
+  const int ncta = (int)gridDim.x, cta = (int)blockIdx.x;
+  for (int f = cta * kMergeWarps + warp; f < nf; f += ncta * kMergeWarps) {
     const float* rows = ws + (size_t)f * chunks * rw;
     const int total = chunks * w;
     // Every global read of the row is requested before any is waited for,
@@ -442,6 +462,31 @@ expand_merge_kernel(const float* __restrict__ ws, int nf, int chunks, int w,
     __syncwarp();
   }
   __syncthreads();
+  if (ncta > 1) {
+    // the grid is one cluster: CTA 0 gathers the other CTAs' row lists, row
+    // f being held by CTA (f / 8) mod ncta, then merges every row
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    if (cta == 0) {
+      for (int o = tid; o < nf * w; o += kMergeThreads) {
+        const int r = (o / w / kMergeWarps) % ncta;
+        if (r != 0) {
+          s_sc[o] = *cluster.map_shared_rank(&s_sc[o], r);
+          s_key[o] = *cluster.map_shared_rank(&s_key[o], r);
+        }
+      }
+      for (int f = tid; f < nf; f += kMergeThreads) {
+        const int r = (f / kMergeWarps) % ncta;
+        if (r != 0) s_front[f] = *cluster.map_shared_rank(&s_front[f], r);
+      }
+      if (tid == 0)
+        for (int r = 1; r < ncta; ++r)
+          if (*cluster.map_shared_rank(&s_bad, r)) s_bad = 1;
+    }
+    cluster.sync();  // every CTA's shared memory stays until CTA 0 has read it
+    if (cta != 0) return;
+    __syncthreads();
+  }
   if (s_bad) {
     if (tid == 0) report(dev_status, TV_ERR_INVALID_ARG);
     for (int k = tid; k < w; k += kMergeThreads) {
@@ -623,9 +668,26 @@ cudaError_t launch_expand(const float* logits, int32_t vocab, int32_t n_frontier
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  return launch_pdl(expand_merge_kernel, dim3(1), dim3(kMergeThreads), kMergeSmem, s,
-                    static_cast<const float*>(ws), n_frontier, pl.chunks, w, frontier, cum,
-                    n_nodes, new_parent, new_token, new_score, dev_status);
+  // one CTA per 8 rows up to a cluster of kMergeCluster, launched as one
+  // cluster under programmatic serialization
+  const int ncta = std::min(kMergeCluster, (n_frontier + kMergeWarps - 1) / kMergeWarps);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ncta);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = kMergeSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = ncta;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = ncta > 1 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, expand_merge_kernel, static_cast<const float*>(ws), n_frontier,
+                            pl.chunks, w, frontier, cum, n_nodes, new_parent, new_token,
+                            new_score, dev_status);
 }
 
 cudaError_t launch_draft_reroot(const int32_t* parent, const int32_t* token, const float* cum,

@@ -57,7 +57,9 @@ def _check_expansion(logits, frontier, cum, w, got):
                                         (16, 128256, 64), (5, 1, 5), (2, 524288, 16), (1, 131072, 64),
                                         # w = 1 over many slices per row (a chain draft)
                                         (1, 128256, 1), (8, 128256, 1), (64, 128256, 1),
-                                        (3, 5000, 1), (128, 3000, 1)])
+                                        (3, 5000, 1), (128, 3000, 1),
+                                        # merge clusters of 2, 5 and 8 CTAs
+                                        (9, 20000, 8), (40, 4099, 8), (100, 128256, 4)])
 @pytest.mark.parametrize("seed", [0, 1])
 def test_expansion_matches_oracle(nf, vocab, w, seed):
     rng = np.random.default_rng(seed)
@@ -146,6 +148,23 @@ def test_bad_frontier_entry_is_reported():
     torch.cuda.synchronize()
     assert int(st.item()) == tvp.TV_ERR_INVALID_ARG
     assert (got["token"].cpu() == -1).all()
+
+
+@pytest.mark.parametrize("bad_row", [3, 30, 39])
+def test_bad_frontier_entry_in_any_merge_cta_is_reported(bad_row):
+    # 40 rows: the merge runs as a cluster of 5 CTAs, row f held by CTA
+    # (f / 8) % 5; a bad entry in any of them must reach CTA 0's check
+    rng = np.random.default_rng(bad_row)
+    nf, vocab = 40, 3000
+    logits = torch.from_numpy(rng.standard_normal((nf, vocab), dtype=np.float32)).to(DEV)
+    frontier = torch.arange(nf, dtype=torch.int32, device=DEV)
+    frontier[bad_row] = nf + 7
+    cum = torch.zeros(nf, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = tvp.tree_expand(logits, frontier, cum, 8, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == tvp.TV_ERR_INVALID_ARG
+    assert (got["token"].cpu() == -1).all() and (got["parent"].cpu() == -1).all()
 
 
 # ---------------------------------------------------------------- re-rooting
