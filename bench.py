@@ -947,10 +947,10 @@ def run_sweep(args, local_rank):
 
 def run_expand(args, local_rank):
     """The draft side alone, at the pages' width: one maximum-likelihood
-    expansion of w = 8 leaves from 8 frontier nodes over a 128256-token
-    vocabulary (float32 logits, 4.1 MB), cycling through enough copies of the
-    logits to exceed L2, then the draft re-root map.  One JSON line."""
-    import numpy as np
+    expansion of w = 8 leaves from 8 frontier nodes (or each count given by
+    --expand-rows) over a 128256-token vocabulary (float32 logits, 4.1 MB
+    for 8 rows), cycling through enough copies of the logits to exceed L2.
+    One JSON line per frontier size."""
     import torch
 
     import speculative_decoding_tree_masked_gb300 as tvp
@@ -959,7 +959,19 @@ def run_expand(args, local_rank):
     dev = torch.device("cuda", local_rank)
     stream = torch.cuda.Stream(dev)
     peaks = _peaks()
-    nf, w, vocab, n_nodes = 8, 8, VOCAB, 64
+    rows = [int(x) for x in args.expand_rows.split(",")] if args.expand_rows else [8]
+    if any(not 1 <= nf <= tvp.MAX_NODES for nf in rows):
+        raise ValueError(f"--expand-rows takes frontier sizes in 1..{tvp.MAX_NODES}")
+    for nf in rows:
+        _time_expand(args, tvp, dev, stream, peaks, nf)
+
+
+def _time_expand(args, tvp, dev, stream, peaks, nf):
+    import numpy as np
+    import torch
+
+    w, vocab = 8, VOCAB
+    n_nodes = max(64, nf)
     rng = np.random.default_rng(args.seed)
     base = torch.from_numpy(rng.standard_normal((nf, vocab), dtype=np.float32) * 3).to(dev)
     copies = max(3, -(-3 * 130_000_000 // (nf * vocab * 4)))
@@ -1371,6 +1383,8 @@ def main():
                     help="time greedy and sampling acceptance instead of the step")
     ap.add_argument("--expand", action="store_true",
                     help="time the draft side's tree expansion instead of the step")
+    ap.add_argument("--expand-rows", default=None,
+                    help="with --expand: comma-separated frontier sizes (1..128; default 8)")
     ap.add_argument("--paged", action="store_true",
                     help="time the attention over paged K/V caches instead of the step")
     ap.add_argument("--lmhead", action="store_true",
