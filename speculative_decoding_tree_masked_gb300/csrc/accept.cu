@@ -40,8 +40,8 @@ __global__ void __cluster_dims__(kArgmaxCluster, 1, 1) __launch_bounds__(kArgmax
 argmax_kernel(const float* __restrict__ logits, int vocab, int32_t* __restrict__ am) {
   __shared__ float s_val[kArgmaxThreads / 32];
   __shared__ int s_idx[kArgmaxThreads / 32];
-  __shared__ float c_val;
-  __shared__ int c_idx;
+  __shared__ float c_val[kArgmaxCluster];  // CTA 0's: every CTA's winner
+  __shared__ int c_idx[kArgmaxCluster];
   // launched under programmatic serialization: the walk that follows may be
   // scheduled now (it waits for this grid); this grid waits for the kernel
   // before it (which may write the logits) before reading anything
@@ -123,19 +123,18 @@ argmax_kernel(const float* __restrict__ logits, int vocab, int32_t* __restrict__
   if (tid == 0) {
     for (int w = 1; w < kArgmaxThreads / 32; ++w)
       if (better(s_val[w], s_idx[w], bv, bi)) { bv = s_val[w]; bi = s_idx[w]; }
-    c_val = bv;
-    c_idx = bi;
+    // each CTA stores its winner into CTA 0's shared memory; the cluster
+    // barrier's release and acquire make the stores visible to CTA 0, and no
+    // CTA reads another's shared memory after it, so one barrier suffices
+    *cluster.map_shared_rank(&c_val[rank], 0) = bv;
+    *cluster.map_shared_rank(&c_idx[rank], 0) = bi;
   }
   cluster.sync();
   if (rank == 0 && tid == 0) {
-    for (int r = 1; r < kArgmaxCluster; ++r) {
-      const float rv = *cluster.map_shared_rank(&c_val, r);
-      const int ri = *cluster.map_shared_rank(&c_idx, r);
-      if (better(rv, ri, bv, bi)) { bv = rv; bi = ri; }
-    }
+    for (int r = 1; r < kArgmaxCluster; ++r)
+      if (better(c_val[r], c_idx[r], bv, bi)) { bv = c_val[r]; bi = c_idx[r]; }
     am[row] = bi == INT_MAX ? 0 : bi;
   }
-  cluster.sync();  // keep every CTA's shared memory alive until CTA 0 has read it
 }
 
 // Request b of a packed batch owns nodes [off[b], off[b + 1]) of every

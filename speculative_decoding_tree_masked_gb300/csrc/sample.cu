@@ -94,8 +94,8 @@ sample_kernel(const float* __restrict__ logits, int vocab, const __grid_constant
               int32_t* __restrict__ sampled) {
   __shared__ float w_m[kSampleWarps], w_s[kSampleWarps];
   __shared__ double w_mass[kSampleWarps];  // each warp's run's mass at the row maximum
-  __shared__ float cta_m;                  // this CTA's maximum, read by the cluster
-  __shared__ double cta_s;                 // its mass at the row maximum
+  __shared__ float all_m[kSampleCluster];  // every CTA's maximum (each CTA writes its own
+  __shared__ double all_s[kSampleCluster]; // entry in every CTA) and mass at the row maximum
   __shared__ float cta_m_row;              // the row maximum
   __shared__ int sel_owner, sel_warp;      // the drawing CTA and warp (-1: none)
   // launched under programmatic serialization: the walk may be scheduled
@@ -177,14 +177,17 @@ sample_kernel(const float* __restrict__ logits, int vocab, const __grid_constant
   if (tid == 0) {
     float cm = -INFINITY;
     for (int k = 0; k < kSampleWarps; ++k) cm = fmaxf(cm, w_m[k]);
-    cta_m = cm;
+    // this CTA's maximum into every CTA's all_m (the barrier's release and
+    // acquire publish the stores): afterwards each reads only its own copy
+#pragma unroll
+    for (int r = 0; r < kSampleCluster; ++r) *cluster.map_shared_rank(&all_m[rank], r) = cm;
   }
   cluster.sync();
   // the row maximum, then every warp's mass and this CTA's mass at it
   if (tid == 0) {
     float M = -INFINITY;
 #pragma unroll
-    for (int r = 0; r < kSampleCluster; ++r) M = fmaxf(M, *cluster.map_shared_rank(&cta_m, r));
+    for (int r = 0; r < kSampleCluster; ++r) M = fmaxf(M, all_m[r]);
     double total = 0.0;
     for (int k2 = 0; k2 < kSampleWarps; ++k2) {
       const double wm = (w_m[k2] == -INFINITY || M == -INFINITY)
@@ -192,7 +195,8 @@ sample_kernel(const float* __restrict__ logits, int vocab, const __grid_constant
       w_mass[k2] = wm;
       total += wm;
     }
-    cta_s = total;
+#pragma unroll
+    for (int r = 0; r < kSampleCluster; ++r) *cluster.map_shared_rank(&all_s[rank], r) = total;
     cta_m_row = M;
   }
   cluster.sync();
@@ -204,7 +208,7 @@ sample_kernel(const float* __restrict__ logits, int vocab, const __grid_constant
     double S = 0.0, P = 0.0, mass[kSampleCluster];
 #pragma unroll
     for (int r = 0; r < kSampleCluster; ++r) {
-      mass[r] = *cluster.map_shared_rank(&cta_s, r);
+      mass[r] = all_s[r];
       S += mass[r];
     }
     const uint64_t x0 = philox4x64_10_x0((uint64_t)(row - jobs.off[job]), jobs.offset[job], 0ull,
@@ -237,8 +241,7 @@ sample_kernel(const float* __restrict__ logits, int vocab, const __grid_constant
     }
     if (last < 0 && rank == 0) sampled[row] = -1;  // every logit is -inf: nothing is drawn
   }
-  // every CTA has read what it needs from the others' shared memory
-  cluster.sync();
+  __syncthreads();
   if (sel_owner != rank || warp != sel_warp) return;
   const float M = cta_m_row;
   // 32 contiguous pieces of the run, one per lane
