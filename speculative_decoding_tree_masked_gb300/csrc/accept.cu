@@ -36,6 +36,17 @@ __device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
   return a > b || (a == b && ia < ib);
 }
 
+// Split cluster barrier around the kernel's work: every thread arrives
+// (relaxed, without waiting) as it starts and waits before its CTA first
+// stores into another CTA's shared memory, so that every CTA of the cluster
+// has started by then; the wait returns at once in practice.
+__device__ __forceinline__ void cluster_arrive_at_start() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_all_started() {
+  asm volatile("barrier.cluster.wait;" ::: "memory");
+}
+
 __global__ void __cluster_dims__(kArgmaxCluster, 1, 1) __launch_bounds__(kArgmaxThreads)
 argmax_kernel(const float* __restrict__ logits, int vocab, int32_t* __restrict__ am) {
   __shared__ float s_val[kArgmaxThreads / 32];
@@ -48,6 +59,7 @@ argmax_kernel(const float* __restrict__ logits, int vocab, int32_t* __restrict__
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   cg::cluster_group cluster = cg::this_cluster();
+  cluster_arrive_at_start();
   const int rank = (int)cluster.block_rank();
   const int row = blockIdx.y;
   const int tid = threadIdx.x;
@@ -120,6 +132,7 @@ argmax_kernel(const float* __restrict__ logits, int vocab, int32_t* __restrict__
   }
   if ((tid & 31) == 0) { s_val[tid >> 5] = bv; s_idx[tid >> 5] = bi; }
   __syncthreads();
+  cluster_wait_all_started();
   if (tid == 0) {
     for (int w = 1; w < kArgmaxThreads / 32; ++w)
       if (better(s_val[w], s_idx[w], bv, bi)) { bv = s_val[w]; bi = s_idx[w]; }

@@ -89,6 +89,17 @@ struct SampleJobs {
   uint64_t offset[kMaxBatch];
 };
 
+// Split cluster barrier around the kernel's work: every thread arrives
+// (relaxed, without waiting) as it starts and waits before its CTA first
+// stores into another CTA's shared memory, so that every CTA of the cluster
+// has started by then; the wait returns at once in practice.
+__device__ __forceinline__ void cluster_arrive_at_start() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_all_started() {
+  asm volatile("barrier.cluster.wait;" ::: "memory");
+}
+
 __global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kSampleThreads)
 sample_kernel(const float* __restrict__ logits, int vocab, const __grid_constant__ SampleJobs jobs,
               int32_t* __restrict__ sampled) {
@@ -104,6 +115,7 @@ sample_kernel(const float* __restrict__ logits, int vocab, const __grid_constant
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ double sel_rem;               // the target mass left inside that warp's run
   cg::cluster_group cluster = cg::this_cluster();
+  cluster_arrive_at_start();
   const int row = blockIdx.y;
   int job = 0;  // the request owning this row
   while (job + 1 < jobs.batch && row >= jobs.off[job + 1]) ++job;
@@ -174,6 +186,7 @@ sample_kernel(const float* __restrict__ logits, int vocab, const __grid_constant
   }
   if (lane == 0) { w_m[warp] = mm; w_s[warp] = ss; }
   __syncthreads();
+  cluster_wait_all_started();
   if (tid == 0) {
     float cm = -INFINITY;
     for (int k = 0; k < kSampleWarps; ++k) cm = fmaxf(cm, w_m[k]);
